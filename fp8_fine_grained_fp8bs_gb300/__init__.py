@@ -1,0 +1,198 @@
+"""Python binding of the fp8bs C ABI (include/fp8bs.h).
+
+Fine-grained FP8 quantisation and block-scaled FP8 GEMM on GB300 (sm_103a),
+after DeepSeek-V3 "Infrastructure" §3.3.  Every step runs in the CUDA
+library ``_build/libfp8bs.so``; this module only marshals arguments
+(tensors -> device pointers, the current torch stream) and turns non-zero
+status codes into exceptions.  There is no CPU path: if the library is
+missing or fails to load, every call raises.
+
+The functions named ``fp8bs_*`` mirror the C entry points one to one and
+take tensors or raw device pointers.  ``quantize_act``, ``quantize_weight``,
+``gemm`` and ``grouped_gemm`` additionally allocate their outputs with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH, build as _build
+
+__all__ = [
+    "Fp8bsError", "load_library", "build",
+    "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
+    "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string",
+    "quantize_act", "quantize_weight", "gemm", "grouped_gemm",
+    "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128",
+]
+
+OUT_F32, OUT_BF16 = 0, 1
+SCALE_BLOCK128x128, SCALE_ROW1x128 = 0, 1
+
+STATUS_NAMES = {0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_SHAPE", 3: "FP8BS_ERR_ALIGNMENT",
+                4: "FP8BS_ERR_UNSUPPORTED_ARCH", 5: "FP8BS_ERR_CUDA", 6: "FP8BS_ERR_TIMEOUT",
+                7: "FP8BS_ERR_DEVICE_ARG"}
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+
+_c_i64, _c_int, _c_vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+_SIGNATURES = {
+    "fp8bs_quantize_act": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp],
+    "fp8bs_quantize_weight": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp],
+    "fp8bs_gemm": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
+    "fp8bs_grouped_gemm": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
+                           _c_vp],
+    "fp8bs_get_device_status": [_c_vp],
+    "fp8bs_set_wait_timeout_ms": [_c_i64],
+    "fp8bs_status_string": [_c_int],
+}
+
+
+def build(force: bool = False) -> str:
+    """Compiles the CUDA library in-tree (nvcc, sm_103a) and returns its path."""
+    return _build(force=force)
+
+
+def load_library(path: str | None = None):
+    """Loads libfp8bs.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"fp8bs CUDA library not built: {p} is missing (run build())")
+            lib = ctypes.CDLL(p, mode=ctypes.RTLD_LOCAL)
+            for name, argtypes in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = ctypes.c_char_p if name == "fp8bs_status_string" else ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise Fp8bsError(status, where)
+
+
+# ------------------------------------------------------------ raw C entry points
+
+def fp8bs_quantize_act(x, M, K, ldx, xq, sx, xq_t=None, sx_t=None, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_quantize_act(_ptr(x), M, K, ldx, _ptr(xq), _ptr(sx), _ptr(xq_t), _ptr(sx_t),
+                                  _stream(stream)), "fp8bs_quantize_act")
+
+
+def fp8bs_quantize_weight(w, N, K, ldw, wq, sw, wq_t=None, sw_t=None, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_quantize_weight(_ptr(w), N, K, ldw, _ptr(wq), _ptr(sw), _ptr(wq_t), _ptr(sw_t),
+                                     _stream(stream)), "fp8bs_quantize_weight")
+
+
+def fp8bs_gemm(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate=0, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), sb_kind, _ptr(d), d_dtype, M, N, K,
+                          int(accumulate), _stream(stream)), "fp8bs_gemm")
+
+
+def fp8bs_grouped_gemm(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N, K, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_grouped_gemm(_ptr(a), _ptr(sa), M_total, _ptr(offsets), num_groups, _ptr(b), _ptr(sb),
+                                  _ptr(d), d_dtype, N, K, _stream(stream)), "fp8bs_grouped_gemm")
+
+
+def fp8bs_get_device_status(stream=None) -> int:
+    return load_library().fp8bs_get_device_status(_stream(stream))
+
+
+def fp8bs_set_wait_timeout_ms(ms: int):
+    _check(load_library().fp8bs_set_wait_timeout_ms(int(ms)), "fp8bs_set_wait_timeout_ms")
+
+
+def fp8bs_status_string(status: int) -> str:
+    return load_library().fp8bs_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------ allocating conveniences
+
+def quantize_act(x, transposed: bool = False, stream=None):
+    """x: [M, K] bfloat16 CUDA tensor (row-major, K % 128 == 0).
+
+    Returns (xq [M,K] uint8, sx [K/128, M] float32) and, with ``transposed``,
+    also (xq_t [K,M] uint8, sx_t [M/128, K] float32).
+    """
+    import torch
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    xq_t = sx_t = None
+    if transposed:
+        xq_t = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+        sx_t = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
+    fp8bs_quantize_act(x, M, K, x.stride(0), xq, sx, xq_t, sx_t, stream)
+    return (xq, sx, xq_t, sx_t) if transposed else (xq, sx)
+
+
+def quantize_weight(w, transposed: bool = False, stream=None):
+    """w: [N, K] bfloat16 CUDA tensor.  Returns (wq, sw[, wq_t, sw_t])."""
+    import torch
+    N, K = w.shape
+    wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    wq_t = sw_t = None
+    if transposed:
+        wq_t = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+        sw_t = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
+    fp8bs_quantize_weight(w, N, K, w.stride(0), wq, sw, wq_t, sw_t, stream)
+    return (wq, sw, wq_t, sw_t) if transposed else (wq, sw)
+
+
+def gemm(a, sa, b, sb, sb_kind: int = SCALE_BLOCK128x128, out_dtype=None, out=None, accumulate: bool = False,
+         stream=None):
+    """D = A B^T with per-128-K-block scales; A [M,K], B [N,K] uint8 E4M3."""
+    import torch
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    d_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    fp8bs_gemm(a, sa, b, sb, sb_kind, out, d_dtype, M, N, K, int(accumulate), stream)
+    return out
+
+
+def grouped_gemm(a, sa, offsets, b, sb, out_dtype=None, out=None, stream=None):
+    """Per-expert D rows = A rows of the expert x B[g]^T; offsets: int32 CUDA tensor [G+1]."""
+    import torch
+    M, K = a.shape
+    G, N, _ = b.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    d_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    fp8bs_grouped_gemm(a, sa, M, offsets, G, b, sb, out, d_dtype, N, K, stream)
+    return out

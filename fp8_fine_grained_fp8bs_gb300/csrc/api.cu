@@ -1,0 +1,172 @@
+// The C ABI of fp8bs (declared in include/fp8bs.h): argument checks, the
+// architecture check, and dispatch to the kernels on the caller's stream.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "fp8bs.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
+  int sm_count = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// FP8BS_OK with the SM count of the current device, or an error status.
+int current_device(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8BS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& info = g_dev[dev];
+  if (info.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    info.checked = (major == 10 && minor == 3) ? 1 : -1;
+    info.sm_count = sms;
+  }
+  if (info.checked < 0) return FP8BS_ERR_UNSUPPORTED_ARCH;
+  *sm_count = info.sm_count;
+  return FP8BS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx, uint8_t* xq_t,
+                       float* sx_t, void* stream) {
+  if (M < 0 || K < 0 || ldx < K) return FP8BS_ERR_INVALID_ARG;
+  if ((xq_t == nullptr) != (sx_t == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (M > 0 && K > 0 && (x == nullptr || xq == nullptr || sx == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (xq_t != nullptr && M % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(xq_t) || (ldx * 2) % 16 != 0) return FP8BS_ERR_ALIGNMENT;
+  if (!aligned16(sx) || !aligned16(sx_t)) return FP8BS_ERR_ALIGNMENT;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  const auto* xb = static_cast<const uint16_t*>(x);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (xq_t != nullptr) return from_cuda(fp8bs::launch_quantize_act_dual(xb, M, K, ldx, xq, sx, xq_t, sx_t, s));
+  return from_cuda(fp8bs::launch_quantize_act_1x128(xb, M, K, ldx, xq, sx, sms, s));
+}
+
+int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw, uint8_t* wq_t,
+                          float* sw_t, void* stream) {
+  if (N < 0 || K < 0 || ldw < K) return FP8BS_ERR_INVALID_ARG;
+  if ((wq_t == nullptr) != (sw_t == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (N > 0 && K > 0 && (w == nullptr || wq == nullptr || sw == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(wq) || !aligned16(wq_t) || (ldw * 2) % 16 != 0) return FP8BS_ERR_ALIGNMENT;
+  if (N == 0 || K == 0) return FP8BS_OK;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_quantize_weight(static_cast<const uint16_t*>(w), N, K, ldw, wq, sw, wq_t, sw_t,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+static int run_gemm(const fp8bs::GemmArgs& args, void* stream) {
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  bool tmap_failed = false, reg_failed = false;
+  const cudaError_t e =
+      fp8bs::launch_gemm(args, sms, static_cast<cudaStream_t>(stream), &tmap_failed, &reg_failed);
+  if (tmap_failed) return FP8BS_ERR_ALIGNMENT;
+  return from_cuda(e);
+}
+
+int fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int sb_kind, void* d,
+               int d_dtype, int64_t M, int64_t N, int64_t K, int accumulate, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (sb_kind != FP8BS_SCALE_BLOCK128x128 && sb_kind != FP8BS_SCALE_ROW1x128) return FP8BS_ERR_INVALID_ARG;
+  if (d_dtype != FP8BS_OUT_F32 && d_dtype != FP8BS_OUT_BF16) return FP8BS_ERR_INVALID_ARG;
+  if (accumulate && d_dtype != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (K == 0) return FP8BS_ERR_SHAPE;
+  if (a == nullptr || sa == nullptr || b == nullptr || sb == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_ERR_ALIGNMENT;
+  if (sb_kind == FP8BS_SCALE_ROW1x128 && !aligned16(sb)) return FP8BS_ERR_ALIGNMENT;
+  fp8bs::GemmArgs g{};
+  g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.d = d; g.offsets = nullptr;
+  g.M = M; g.N = N; g.K = K; g.num_groups = 1; g.grouped = false;
+  g.sb_row = sb_kind == FP8BS_SCALE_ROW1x128;
+  g.out_bf16 = d_dtype == FP8BS_OUT_BF16;
+  g.accumulate = accumulate != 0;
+  g.timeout_ns = g_timeout_ns.load();
+  return run_gemm(g, stream);
+}
+
+int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets, int num_groups,
+                       const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N, int64_t K, void* stream) {
+  if (M_total < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (num_groups < 1 || num_groups > 1024) return FP8BS_ERR_INVALID_ARG;
+  if (d_dtype != FP8BS_OUT_F32 && d_dtype != FP8BS_OUT_BF16) return FP8BS_ERR_INVALID_ARG;
+  if (offsets == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M_total > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 24) || K > (int64_t(1) << 24))
+    return FP8BS_ERR_SHAPE;
+  if (M_total == 0 || N == 0) return FP8BS_OK;
+  if (K == 0) return FP8BS_ERR_SHAPE;
+  if (a == nullptr || sa == nullptr || b == nullptr || sb == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_ERR_ALIGNMENT;
+  fp8bs::GemmArgs g{};
+  g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.d = d; g.offsets = offsets;
+  g.M = M_total; g.N = N; g.K = K; g.num_groups = num_groups; g.grouped = true;
+  g.sb_row = false;
+  g.out_bf16 = d_dtype == FP8BS_OUT_BF16;
+  g.accumulate = false;
+  g.timeout_ns = g_timeout_ns.load();
+  return run_gemm(g, stream);
+}
+
+int fp8bs_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+  int v = 0;
+  if (fp8bs::gemm_take_status(&v) != cudaSuccess) return FP8BS_ERR_CUDA;
+  return v;
+}
+
+int fp8bs_set_wait_timeout_ms(int64_t ms) {
+  if (ms < 0) return FP8BS_ERR_INVALID_ARG;
+  g_timeout_ns.store(ms == 0 ? kDefaultTimeoutNs : static_cast<uint64_t>(ms) * 1000000ull);
+  return FP8BS_OK;
+}
+
+const char* fp8bs_status_string(int status) {
+  switch (status) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+    case FP8BS_ERR_SHAPE: return "shape breaks a multiple-of-128 rule";
+    case FP8BS_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+    case FP8BS_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103";
+    case FP8BS_ERR_CUDA: return "CUDA call failed";
+    case FP8BS_ERR_TIMEOUT: return "a bounded device wait expired";
+    case FP8BS_ERR_DEVICE_ARG: return "invalid device-resident argument (group offsets)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

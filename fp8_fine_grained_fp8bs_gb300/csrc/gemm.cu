@@ -1,0 +1,498 @@
+// Block-scaled FP8 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// D[m][n] = sum_kb P_kb[m][n] * s_a[m][kb] * s_b(n, kb), where P_kb is the
+// E4M3 x E4M3 product over one 128-wide block of K.  This is the
+// "increasing accumulation precision" scheme of DeepSeek-V3 §3.3.2 / Figure
+// 7b (every N_C = 128 elements the tensor-core partial is promoted to FP32,
+// multiplied by the two scales and accumulated; §3.5.2 names the cost of
+// that data movement), mapped onto Blackwell:
+//
+//   * a persistent, warp-specialised CTA per SM: warp 0 issues TMA loads of
+//     128x128 A and BNx128 B tiles into a shared-memory ring; warp 1 issues
+//     the MMAs (4 x tcgen05.mma K=32 per 128-K block) into one of two TMEM
+//     partial buffers, the first of the four overwriting the buffer; warps
+//     4-11 (two warpgroups) fold each finished partial into FP32 registers
+//     with the block's scale (acc += P_kb * s_a * s_b) while the tensor core
+//     already computes the next block into the other buffer;
+//   * the running FP32 accumulator never leaves the registers; each thread
+//     owns one output row (its TMEM lane) and BN/2 columns;
+//   * mbarrier pipelines (smem ring full/empty, TMEM full/empty) with
+//     bounded waits; a timeout records a status and unwinds.
+//
+// The same kernel serves the dense GEMM (one group) and the grouped MoE
+// GEMM (per-expert row segments whose offsets are multiples of 128, read
+// from device memory; the expert index selects B's slice through a 3-D
+// tensor map).
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8bs {
+namespace {
+
+__device__ int g_gemm_status;
+
+constexpr int kThreads = 384;        // 12 warps
+constexpr int kEpiWarp0 = 4;         // warps 4..11 fold and store
+constexpr int kEpiThreads = 256;
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 128;         // = N_C
+constexpr int kUmmaK = 32;           // K of one kind::f8f6f4 MMA (bytes of E4M3)
+constexpr int kMaxGroups = 1024;
+constexpr uint32_t kTmemCols = 512;  // two partial buffers of up to 256 columns
+constexpr uint32_t kRegsProducer = 56;
+constexpr uint32_t kRegsEpilogue = 224;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = kBlockM * kBlockK;       // 16 KB
+  static constexpr int kBBytes = BN * kBlockK;            // 16 or 32 KB
+  static constexpr int kScaleBytes = BN * 4;              // per-column B scales of one stage
+  static constexpr int kColsPerThread = BN / 2;
+  static constexpr int kChunks = kColsPerThread / 32;
+  // dynamic shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffScale = kOffB + kStages * kBBytes;
+  static constexpr int kOffBar = kOffScale + kStages * kScaleBytes;
+  static constexpr int kNumBars = 4 * kStages + 4 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;       // tmem slot, abort flag, tile count
+  static constexpr int kOffGroups = kOffMisc + 16;              // offsets[G+1], cum[G+1]
+  static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
+};
+
+struct KParams {
+  const float* sa;
+  const float* sb;
+  void* d;
+  const int32_t* offsets;
+  int64_t M;
+  int N;
+  int nkb;
+  int num_groups;
+  int out_bf16;
+  int accumulate;
+  uint64_t timeout_ns;
+};
+
+// Two float32 -> BF16x2 (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_status, 0, code); }
+
+// Tile t -> (first row, first column, group).  Tiles run m-tile-major with
+// the BN-wide n-tiles of one m-tile consecutive, so concurrently running
+// CTAs share A rows.
+template <int BN>
+__device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const int* s_off, const int* s_cum,
+                                            int num_groups, int& row0, int& n0, int& g) {
+  const int mt = t / ntn;
+  n0 = (t - mt * ntn) * BN;
+  if (!grouped) {
+    g = 0;
+    row0 = mt * kBlockM;
+    return;
+  }
+  int lo = 0, hi = num_groups - 1;  // last g with cum[g] <= mt
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_cum[mid] <= mt) lo = mid; else hi = mid - 1;
+  }
+  g = lo;
+  row0 = s_off[g] + (mt - s_cum[g]) * kBlockM;
+}
+
+template <int BN, bool kRowScale, bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + C::kOffA;
+  uint8_t* sB = smem + C::kOffB;
+  float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;                       // [kStages] TMA -> MMA
+  uint64_t* empty = bars + C::kStages;         // [kStages] MMA -> TMA
+  uint64_t* sc_full = bars + 2 * C::kStages;   // [kStages] per-column B scales landed
+  uint64_t* sc_empty = bars + 3 * C::kStages;  // [kStages] epilogue done with them
+  uint64_t* t_full = bars + 4 * C::kStages;    // [2] partial ready in TMEM
+  uint64_t* t_empty = t_full + 2;              // [2] partial consumed
+  uint64_t* teardown = t_full + 4;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  int* s_off = reinterpret_cast<int*>(smem + C::kOffGroups);
+  int* s_cum = s_off + (kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ntn = (p.N + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sc_full[s], 1);
+      mbar_init(&sc_empty[s], kEpiThreads / 32);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&t_full[b], 1);
+      mbar_init(&t_empty[b], kEpiThreads);
+    }
+    mbar_init(teardown, 1);
+    fence_barrier_init();
+    // tile count (and, for the grouped GEMM, the validated group table)
+    int total_mt = 0;
+    bool ok = true;
+    if (kGrouped) {
+      int prev = 0;
+      for (int g = 0; g <= p.num_groups; ++g) {
+        const int o = p.offsets[g];
+        ok = ok && (o >= prev || g == 0) && o >= 0 && (o % kBlockM) == 0 && o <= p.M;
+        s_off[g] = o;
+        prev = o;
+      }
+      if (ok) {
+        for (int g = 0; g < p.num_groups; ++g) {
+          s_cum[g] = total_mt;
+          total_mt += (s_off[g + 1] - s_off[g]) / kBlockM;
+        }
+        s_cum[p.num_groups] = total_mt;
+      } else {
+        record_status(kStatusDeviceArg);
+        total_mt = 0;
+      }
+    } else {
+      total_mt = static_cast<int>((p.M + kBlockM - 1) / kBlockM);
+    }
+    misc[1] = 0;  // abort flag
+    misc[2] = static_cast<uint32_t>(total_mt * ntn);
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&misc[0], kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = misc[0];
+  const int total_tiles = static_cast<int>(misc[2]);
+  volatile uint32_t* abort_flag = &misc[1];
+
+  if (warp < kEpiWarp0) {
+    setmaxnreg_dec<kRegsProducer>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool live = true;
+      int issued = 0;
+      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+        int row0, n0, g;
+        tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
+          mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
+          tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBlockK, row0);
+          if (kGrouped)
+            tma_load_3d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0, g);
+          else
+            tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0);
+          if (kRowScale) {
+            if (!mbar_wait(&sc_empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
+            const int cols = min(BN, p.N - n0);
+            mbar_arrive_expect_tx(&sc_full[stage], cols * 4);
+            bulk_load(sScale + stage * BN, p.sb + static_cast<int64_t>(kb) * p.N + n0, cols * 4, &sc_full[stage]);
+          }
+          ++issued;
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!live) {
+        record_status(kStatusTimeout);
+        *abort_flag = 1;
+        // let the copies already issued land before the CTA can exit
+        for (int s = 0; s < C::kStages && s < issued; ++s) {
+          int st = stage - 1 - s;
+          uint32_t ph = phase;
+          if (st < 0) { st += C::kStages; ph ^= 1; }
+          (void)mbar_wait(&full[st], ph, p.timeout_ns);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t buf = 0, tphase = 0;
+      bool live = true;
+      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.timeout_ns)) { live = false; break; }
+          if (!mbar_wait(&t_empty[buf], tphase ^ 1, p.timeout_ns)) { live = false; break; }
+          tc_fence_after_sync();
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint32_t dtmem = tmem_base + buf * BN;
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k)
+            mma_e4m3(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          mma_commit(&t_full[buf]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          buf ^= 1;
+          if (buf == 0) tphase ^= 1;
+        }
+      }
+      if (!live) {
+        record_status(kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // wait for every MMA issued so far before TMEM can be released
+      mma_commit(teardown);
+      (void)mbar_wait(teardown, 0, p.timeout_ns);
+    }
+  } else {
+    setmaxnreg_inc<kRegsEpilogue>();
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - kEpiWarp0;      // 0..7
+    const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
+    const int colhalf = e >> 2;          // which BN/2 columns
+    uint32_t buf = 0, tphase = 0;
+    int sstage = 0;
+    uint32_t sphase = 0;
+    bool live = true;
+    for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+      int row0, n0, g;
+      tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
+      const int64_t m = static_cast<int64_t>(row0) + quarter * 32 + lane;
+      const bool mvalid = m < p.M;
+      const int ncol0 = n0 + colhalf * C::kColsPerThread;
+      const float* sbp = nullptr;
+      if (!kRowScale)
+        sbp = p.sb + (static_cast<int64_t>(g) * ((p.N + kGroup - 1) / kGroup) + ncol0 / kGroup) * p.nkb;
+      float acc[C::kColsPerThread];
+#pragma unroll
+      for (int j = 0; j < C::kColsPerThread; ++j) acc[j] = 0.0f;
+      float sa_next = mvalid ? __ldg(p.sa + m) : 0.0f;
+      float sb_next = (!kRowScale && ncol0 < p.N) ? __ldg(sbp) : 0.0f;
+      for (int kb = 0; kb < p.nkb; ++kb) {
+        const float sa_cur = sa_next;
+        const float sb_cur = sb_next;
+        if (kb + 1 < p.nkb) {
+          sa_next = mvalid ? __ldg(p.sa + static_cast<int64_t>(kb + 1) * p.M + m) : 0.0f;
+          if (!kRowScale && ncol0 < p.N) sb_next = __ldg(sbp + kb + 1);
+        }
+        if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
+        if (kRowScale && !mbar_wait(&sc_full[sstage], sphase, p.timeout_ns)) { live = false; break; }
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
+                               colhalf * C::kColsPerThread;
+        const float s_ab = sa_cur * sb_cur;
+#pragma unroll
+        for (int ch = 0; ch < C::kChunks; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(taddr + ch * 32, r);
+          tmem_wait_ld(r);
+          if (kRowScale) {
+            const float4* sc4 = reinterpret_cast<const float4*>(sScale + sstage * BN + colhalf * C::kColsPerThread +
+                                                                ch * 32);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 sc = sc4[j4];
+              acc[ch * 32 + 4 * j4 + 0] = fmaf(__uint_as_float(r[4 * j4 + 0]), sa_cur * sc.x, acc[ch * 32 + 4 * j4 + 0]);
+              acc[ch * 32 + 4 * j4 + 1] = fmaf(__uint_as_float(r[4 * j4 + 1]), sa_cur * sc.y, acc[ch * 32 + 4 * j4 + 1]);
+              acc[ch * 32 + 4 * j4 + 2] = fmaf(__uint_as_float(r[4 * j4 + 2]), sa_cur * sc.z, acc[ch * 32 + 4 * j4 + 2]);
+              acc[ch * 32 + 4 * j4 + 3] = fmaf(__uint_as_float(r[4 * j4 + 3]), sa_cur * sc.w, acc[ch * 32 + 4 * j4 + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), s_ab, acc[ch * 32 + j]);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&t_empty[buf]);
+        if (kRowScale) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sc_empty[sstage]);
+          if (++sstage == C::kStages) { sstage = 0; sphase ^= 1; }
+        }
+        buf ^= 1;
+        if (buf == 0) tphase ^= 1;
+      }
+      if (!live) break;
+      // ---- store this thread's row segment
+      if (mvalid && ncol0 < p.N) {
+        if (p.out_bf16) {
+          __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) + m * p.N + ncol0;
+#pragma unroll
+          for (int j = 0; j < C::kColsPerThread; j += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+            *reinterpret_cast<uint4*>(drow + j) = v;
+          }
+        } else {
+          float* drow = reinterpret_cast<float*>(p.d) + m * p.N + ncol0;
+#pragma unroll
+          for (int j = 0; j < C::kColsPerThread; j += 4) {
+            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            if (p.accumulate) {
+              const float4 o = *reinterpret_cast<const float4*>(drow + j);
+              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *reinterpret_cast<float4*>(drow + j) = v;
+          }
+        }
+      }
+    }
+    if (!live) {
+      record_status(kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// --------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// K-major E4M3 operand [outer...][inner=K] with a 128 x box_rows box and
+// 128-byte swizzling (one 128-byte row of K per box row).
+bool encode_operand(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                    uint32_t box_rows) {
+  auto enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t gdim[3];
+  cuuint64_t gstride[2];
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) gstride[i] = strides[i];
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gdim, gstride,
+          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool kRowScale, bool kGrouped>
+cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap_failed, bool* reg_check_failed) {
+  using C = Cfg<BN>;
+  auto kern = gemm_kernel<BN, kRowScale, kGrouped>;
+  // The register split (warps 0-3 shrink to kRegsProducer, warps 4-11 grow
+  // to kRegsEpilogue) must fit in what the CTA is launched with.
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, kern);
+  if (err != cudaSuccess) return err;
+  if (static_cast<int64_t>(attr.numRegs) * kThreads <
+      static_cast<int64_t>(kRegsProducer) * 128 + static_cast<int64_t>(kRegsEpilogue) * kEpiThreads) {
+    *reg_check_failed = true;
+    return cudaErrorInvalidConfiguration;
+  }
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+
+  CUtensorMap tmA, tmB;
+  const uint64_t dA[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+  const uint64_t sA[1] = {static_cast<uint64_t>(a.K)};
+  if (!encode_operand(&tmA, a.a, 2, dA, sA, kBlockM)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+  if (kGrouped) {
+    const uint64_t dB[3] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N),
+                            static_cast<uint64_t>(a.num_groups)};
+    const uint64_t sB[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.K) * a.N};
+    if (!encode_operand(&tmB, a.b, 3, dB, sB, BN)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+  } else {
+    const uint64_t dB[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N)};
+    const uint64_t sB[1] = {static_cast<uint64_t>(a.K)};
+    if (!encode_operand(&tmB, a.b, 2, dB, sB, BN)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+  }
+
+  KParams kp;
+  kp.sa = a.sa;
+  kp.sb = a.sb;
+  kp.d = a.d;
+  kp.offsets = a.offsets;
+  kp.M = a.M;
+  kp.N = static_cast<int>(a.N);
+  kp.nkb = static_cast<int>(a.K / kBlockK);
+  kp.num_groups = a.num_groups;
+  kp.out_bf16 = a.out_bf16 ? 1 : 0;
+  kp.accumulate = a.accumulate ? 1 : 0;
+  kp.timeout_ns = a.timeout_ns;
+
+  // Persistent grid: one CTA per SM, or fewer when there are fewer tiles.
+  // (The grouped tile count lives on the device; the grid covers its bound.)
+  const int64_t ntn = (a.N + BN - 1) / BN;
+  const int64_t mt_bound = kGrouped ? (a.M / kBlockM + a.num_groups) : (a.M + kBlockM - 1) / kBlockM;
+  const int64_t tiles = mt_bound * ntn;
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap_failed,
+                        bool* reg_check_failed) {
+  *tmap_failed = false;
+  *reg_check_failed = false;
+  // 128-wide n-tiles when 256-wide ones would leave most SMs idle.
+  const int64_t mt = (a.M + kBlockM - 1) / kBlockM;
+  const bool narrow = a.N <= 128 || (!a.grouped && mt * ((a.N + 255) / 256) < sm_count);
+  if (a.grouped) {
+    if (a.sb_row) return cudaErrorInvalidValue;
+    return narrow ? run<128, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                  : run<256, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
+  }
+  if (a.sb_row)
+    return narrow ? run<128, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                  : run<256, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
+  return narrow ? run<128, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                : run<256, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
+}
+
+cudaError_t gemm_take_status(int* status) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int));
+  }
+  *status = v;
+  return e;
+}
+
+}  // namespace fp8bs

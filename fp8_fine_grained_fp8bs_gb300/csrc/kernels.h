@@ -1,0 +1,47 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+// ---- quantize.cu
+cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                      float* sx, int sm_count, cudaStream_t stream);
+cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                     float* sx, uint8_t* xq_t, float* sx_t, cudaStream_t stream);
+cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
+                                   float* sw, uint8_t* wq_t, float* sw_t, cudaStream_t stream);
+
+// ---- gemm.cu
+struct GemmArgs {
+  const uint8_t* a;        // [M][K] E4M3, K-major
+  const float* sa;         // [K/128][M] kb-major
+  const uint8_t* b;        // [G][N][K] E4M3 (G = 1 for the dense GEMM)
+  const float* sb;         // block: [G][N/128][K/128]; row: [K/128][N]
+  void* d;                 // [M][N]
+  const int32_t* offsets;  // grouped only: device [G+1]
+  int64_t M;               // rows of A (M_total for the grouped GEMM)
+  int64_t N, K;
+  int num_groups;          // 1 for the dense GEMM
+  bool grouped;
+  bool sb_row;             // FP8BS_SCALE_ROW1x128
+  bool out_bf16;
+  bool accumulate;
+  uint64_t timeout_ns;
+};
+
+// Returns cudaSuccess, or an error; *tmap_failed is set when a tensor map
+// could not be encoded, *reg_check_failed when the compiled kernel's
+// register count does not match the warp-specialised register split.
+cudaError_t launch_gemm(const GemmArgs& args, int sm_count, cudaStream_t stream, bool* tmap_failed,
+                        bool* reg_check_failed);
+
+// Reads and clears the device status word of the GEMM kernels (the only
+// kernels with waits or device-side argument checks); synchronous copy on
+// the current device.
+cudaError_t gemm_take_status(int* status);
+
+}  // namespace fp8bs

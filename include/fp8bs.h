@@ -1,0 +1,172 @@
+/*
+ * fp8bs — fine-grained FP8 quantisation and block-scaled FP8 GEMM for
+ * NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * The method is DeepSeek-V3's FP8 training scheme ("Infrastructure" §3.3):
+ *   - §3.3.2 "fine-grained quantization": activations are scaled per 1x128
+ *     tile (one token, 128 channels), weights per 128x128 block, and the
+ *     scales vary along the GEMM's inner dimension;
+ *   - §3.3.2 "online quantization": the max absolute value of each tile or
+ *     block is computed when the tensor is used;
+ *   - §3.3.2 "mantissa over exponents": every tensor is E4M3;
+ *   - §3.3.2 "increasing accumulation precision" (Figure 7b): every
+ *     N_C = 128 elements of K the tensor-core partial sum is promoted to
+ *     FP32, multiplied by the two scales and accumulated;
+ *   - the explicit formulas are the Figure 7 explainer's ("DeepSeek-V3 FP8
+ *     动态量化", "Fine-grained quantization"): s = absmax / F_max,
+ *     FP8(x) = round(x / s), out += MMA(FP8(x), FP8(w)) * s_x * s_w.
+ * Precise readings used here: F_max = 448 (largest finite E4M3, OCP "FN"
+ * encoding); round = nearest-even with saturation to +-448; x / s is an IEEE
+ * float32 division; the stored scale is s as float32; a group whose absmax
+ * is 0 gets s = 0 and all-zero codes.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory and never synchronises, except
+ *     fp8bs_get_device_status().  Every call is asynchronous on `stream`
+ *     (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Matrices are row-major.  BF16 is IEEE bfloat16 (uint16 bit patterns),
+ *     E4M3 codes are bytes, scales are float32.
+ *   - "kb-major" scale layout: the scale of row r and 128-column group kb
+ *     is stored at s[kb * rows + r] (the rows of one group are contiguous).
+ *   - Argument errors are returned before anything is launched.  All device
+ *     pointers must be 16-byte aligned, every leading dimension in bytes a
+ *     multiple of 16.  The current device must have compute capability
+ *     10.3 (FP8BS_ERR_UNSUPPORTED_ARCH otherwise).
+ *   - Every wait inside a kernel is bounded in time; a wait that expires, or
+ *     a device-side argument check that fails, records a status that
+ *     fp8bs_get_device_status() returns.
+ *   - Inputs holding NaN or Inf are outside the contract.
+ */
+#ifndef FP8BS_H_
+#define FP8BS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8BS_OK = 0,
+  FP8BS_ERR_INVALID_ARG = 1,      /* NULL pointer, negative size, unknown enum value */
+  FP8BS_ERR_SHAPE = 2,            /* a size breaks a multiple-of-128 rule */
+  FP8BS_ERR_ALIGNMENT = 3,        /* pointer or leading dimension not 16-byte aligned */
+  FP8BS_ERR_UNSUPPORTED_ARCH = 4, /* current device is not sm_103 */
+  FP8BS_ERR_CUDA = 5,             /* a CUDA runtime or driver call failed */
+  FP8BS_ERR_TIMEOUT = 6,          /* a bounded device wait expired */
+  FP8BS_ERR_DEVICE_ARG = 7        /* a device-resident argument (group offsets) was invalid */
+} fp8bs_status;
+
+typedef enum { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 } fp8bs_out_dtype;
+
+typedef enum {
+  /* B's scale is per 128x128 block: sb[(n / 128) * (K / 128) + kb], i.e. a
+   * row-major [ceil(N/128)][K/128] array (weights, §3.3.2 (2)). */
+  FP8BS_SCALE_BLOCK128x128 = 0,
+  /* B's scale is per row and 1x128 group, kb-major: sb[kb * N + n] (both
+   * operands are activations, as in the Wgrad GEMM, §3.3.1 / Figure 6). */
+  FP8BS_SCALE_ROW1x128 = 1
+} fp8bs_b_scale_kind;
+
+/*
+ * Activation quantisation, 1x128 tiles (§3.3.2 "fine-grained quantization"
+ * (1) and "online quantization"), optionally also 128x1 tiles of the same
+ * input (§3.3.3 "low-precision activations" (1): the backward pass needs the
+ * activations grouped along tokens; here they are quantised directly from
+ * BF16 in the same pass).
+ *
+ *   x     [M][ldx] BF16, K columns used.                       (in)
+ *   xq    [M][K]   E4M3 codes of the 1x128 tiles.              (out)
+ *   sx    [K/128][M] float32, kb-major: sx[kb*M + m].          (out)
+ *   xq_t  [K][M]   E4M3 codes of X^T grouped 1x128 along M,    (out, optional)
+ *                  i.e. of the 128x1 tiles of X.
+ *   sx_t  [M/128][K] float32, kb-major: sx_t[tb*K + k] is the   (out, optional)
+ *                  scale of column k, rows 128*tb .. 128*tb+127.
+ * Rules: K % 128 == 0; M >= 0 arbitrary, but M % 128 == 0 when xq_t/sx_t
+ * are given (both or neither).  ldx >= K, ldx*2 % 16 == 0.
+ * Codes and scales are bit-exact with the rule: s = fl32(absmax / 448),
+ * code = E4M3_rne_satfinite(fl32(x / s)), s == 0 -> codes 0.
+ */
+int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx,
+                       uint8_t* xq, float* sx, uint8_t* xq_t, float* sx_t,
+                       void* stream);
+
+/*
+ * Weight quantisation, 128x128 blocks (§3.3.2 "fine-grained quantization"
+ * (2); weights are quantised online too, "online quantization").
+ *
+ *   w     [N][ldw] BF16, K columns used.                        (in)
+ *   wq    [N][K]   E4M3 codes.                                  (out)
+ *   sw    [N/128][K/128] float32, row-major.                    (out)
+ *   wq_t  [K][N]   the same codes transposed (optional): B operand of a  (out)
+ *                  GEMM that uses the weight transposed (Dgrad, Figure 6).
+ *   sw_t  [K/128][N/128] the scales transposed (optional, with wq_t).     (out)
+ * Rules: N % 128 == 0, K % 128 == 0, ldw >= K, ldw*2 % 16 == 0.
+ */
+int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw,
+                          uint8_t* wq, float* sw, uint8_t* wq_t, float* sw_t,
+                          void* stream);
+
+/*
+ * Block-scaled FP8 GEMM, D = A * B^T with per-128-K-block dequantisation
+ * (§3.3.2 "increasing accumulation precision", Figure 7b; Figure 7 explainer
+ * formula out += MMA(FP8(x), FP8(w)) * s_x * s_w):
+ *
+ *   D[m][n] (+)= sum_kb  P_kb[m][n] * sa[kb*M + m] * s_b(n, kb),
+ *   P_kb[m][n]  = sum_{k in 128*kb .. 128*kb+127} A[m][k] * B[n][k]
+ * with P_kb computed on the tensor cores and the scaled sum in FP32.
+ *
+ *   a   [M][K] E4M3, K-major.   sa [K/128][M] float32, kb-major.
+ *   b   [N][K] E4M3, K-major.   sb per sb_kind (see fp8bs_b_scale_kind).
+ *   d   [M][N] FP32 or BF16 (round-to-nearest-even from FP32).
+ *   accumulate: FP32 output only; non-zero -> D += result (Wgrad
+ *   accumulation), zero -> D = result.
+ * Rules: K % 128 == 0, K > 0; N % 128 == 0; M >= 0 arbitrary.
+ */
+int fp8bs_gemm(const uint8_t* a, const float* sa,
+               const uint8_t* b, const float* sb, int sb_kind,
+               void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+               int accumulate, void* stream);
+
+/*
+ * Grouped block-scaled FP8 GEMM for MoE experts (the expert GEMMs consume
+ * FP8 activations dispatched per expert, §3.3.3 "low-precision
+ * communication").  Rows [offsets[g], offsets[g+1]) of A belong to expert
+ * g and are multiplied by expert g's weight:
+ *
+ *   D[r][n] = sum_kb P_kb[r][n] * sa[kb*M_total + r] * sb[g][n/128][kb]
+ *
+ *   a        [M_total][K] E4M3.  sa [K/128][M_total] float32, kb-major.
+ *   offsets  DEVICE int32 [num_groups + 1]: non-decreasing, offsets[0] >= 0,
+ *            every offset a multiple of 128, offsets[G] <= M_total.  Checked
+ *            on the device: a violation skips the launch's work and records
+ *            FP8BS_ERR_DEVICE_ARG.
+ *   b        [num_groups][N][K] E4M3.  sb [num_groups][N/128][K/128].
+ *   d        [M_total][N] FP32 or BF16; rows outside every group are not written.
+ * Rules: K % 128 == 0, N % 128 == 0, 1 <= num_groups <= 1024.
+ */
+int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total,
+                       const int32_t* offsets, int num_groups,
+                       const uint8_t* b, const float* sb,
+                       void* d, int d_dtype, int64_t N, int64_t K, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status of the
+ * current device: FP8BS_OK, FP8BS_ERR_TIMEOUT, FP8BS_ERR_DEVICE_ARG, or
+ * FP8BS_ERR_CUDA if the synchronisation itself failed.
+ */
+int fp8bs_get_device_status(void* stream);
+
+/* Sets the limit of every bounded device wait, in milliseconds (default
+ * 2000; 0 restores the default).  Applies to launches made after the call. */
+int fp8bs_set_wait_timeout_ms(int64_t ms);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fp8bs_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H_ */

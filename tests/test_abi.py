@@ -1,0 +1,109 @@
+"""The C-ABI library builds, loads, exports every entry point declared in
+include/fp8bs.h, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_fine_grained_fp8bs_gb300 as fp8bs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fname in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fname.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fname)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(fp8bs_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fp8bs.build()
+    return fp8bs.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_only_the_abi_is_exported(lib):
+    out = os.popen(f"nm -D --defined-only {fp8bs.build()}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert exported == set(_declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert fp8bs.fp8bs_status_string(s) not in ("", "unknown status")
+    assert fp8bs.fp8bs_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced: every call below fails its checks first
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, -1, 128, 128, FAKE, FAKE, None, None, None), 1),
+    ((FAKE, 128, 100, 128, FAKE, FAKE, None, None, None), 2),
+    ((FAKE, 100, 128, 128, FAKE, FAKE, FAKE, FAKE, None), 2),      # 128x1 needs M % 128 == 0
+    ((FAKE, 128, 128, 128, FAKE, FAKE, FAKE, None, None), 1),      # xq_t without sx_t
+    ((FAKE + 2, 128, 128, 128, FAKE, FAKE, None, None, None), 3),
+    ((FAKE, 128, 128, 132, FAKE, FAKE, None, None, None), 3),      # ldx * 2 not a multiple of 16
+    ((FAKE, 128, 256, 128, FAKE, FAKE, None, None, None), 1),      # ldx < K
+    ((None, 128, 128, 128, FAKE, FAKE, None, None, None), 1),
+])
+def test_quantize_act_argument_errors(lib, args, status):
+    assert lib.fp8bs_quantize_act(*args) == status
+
+
+def test_quantize_weight_argument_errors(lib):
+    assert lib.fp8bs_quantize_weight(FAKE, 100, 128, 128, FAKE, FAKE, None, None, None) == 2
+    assert lib.fp8bs_quantize_weight(FAKE, 128, 128, 128, FAKE, FAKE, FAKE, None, None) == 1
+    assert lib.fp8bs_quantize_weight(FAKE, 128, 128, 128, FAKE + 8, FAKE, None, None, None) == 3
+
+
+def test_gemm_argument_errors(lib):
+    g = lib.fp8bs_gemm
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 100, 0, None) == 2   # K % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 100, 128, 0, None) == 2   # N % 128
+    assert g(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 0, 128, 128, 128, 0, None) == 1   # scale kind
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 5, 128, 128, 128, 0, None) == 1   # output dtype
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 128, 128, 128, 1, None) == 1   # accumulate needs FP32
+    assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 0, 0, None) == 2     # K == 0
+    assert g(FAKE + 4, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 128, 0, None) == 3
+    assert g(None, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 128, 0, None) == 1
+    assert g(None, None, None, None, 0, None, 0, 0, 128, 128, 0, None) == 0     # empty: no-op
+
+
+def test_grouped_gemm_argument_errors(lib):
+    g = lib.fp8bs_grouped_gemm
+    assert g(FAKE, FAKE, 256, FAKE, 0, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # no groups
+    assert g(FAKE, FAKE, 256, FAKE, 1025, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1
+    assert g(FAKE, FAKE, 256, None, 2, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # offsets missing
+    assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE, 0, 128, 100, None) == 2
+    assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
+
+
+def test_timeout_setting(lib):
+    assert lib.fp8bs_set_wait_timeout_ms(-1) == 1
+    assert lib.fp8bs_set_wait_timeout_ms(500) == 0
+    assert lib.fp8bs_set_wait_timeout_ms(0) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import importlib
+    mod = importlib.import_module("fp8_fine_grained_fp8bs_gb300")
+    with pytest.raises(RuntimeError):
+        saved = mod._lib
+        mod._lib = None
+        try:
+            mod.load_library(str(tmp_path / "nope.so"))
+        finally:
+            mod._lib = saved
