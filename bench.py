@@ -1,0 +1,379 @@
+"""Benchmark of the fine-grained FP8 hot path on GB300.
+
+One step = the FP8 Linear forward of the dense workload with online
+quantisation (DeepSeek-V3 §3.3): quantise X[4096,7168] (BF16, 1x128 tiles),
+quantise W[7168,7168] (BF16, 128x128 blocks), block-scaled FP8 GEMM
+Y = X W^T with BF16 output.  ``value`` is the step's GEMM FLOPs
+(2*M*N*K) per second over the whole step, in TFLOP/s.  Measured in the same
+run and reported beside it:
+  * ``gemm``:     the GEMM kernel alone (CUDA events around each launch);
+  * ``quantize``: the standalone 1x128 quantisation of X[16384,7168]
+                  (algorithmic bytes 2 + 1 + 4/128 per element), GB/s;
+  * ``roofline``: the GEMM against the FP8 dense tensor peak;
+  * ``e2e``:      the step through the public API with host buffers (pinned
+                  host -> device copies of X and W, device -> host copy of Y);
+  * ``cpu_baseline``: the CPU oracle on a bounded sample of the same step.
+
+Multi-GPU: every rank runs its own replica on its own batch (data
+parallel, no collective on the data path); ``value`` sums all ranks' FLOPs
+over the slowest rank's time ("scaling": "weak").
+
+``--impl reference`` times the CPU oracle (the reference arm of this
+method: the pages publish no code) on the same metric and prints its line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M, N, K = 4096, 7168, 7168
+QM, QK = 16384, 7168
+GEMM_FLOP = 2.0 * M * N * K
+QUANT_BYTES = QM * QK * (2 + 1 + 4 / 128)
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% of FP8 peak); 1x128 quantize HBM GB/s"
+WORKLOAD = ("dense fprop: quantize X[4096,7168] 1x128 + W[7168,7168] 128x128 to E4M3, "
+            "block-scaled FP8 GEMM Y=X W^T BF16 out; plus standalone quantize of X[16384,7168]")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0      # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _traffic(kernel_key: str, source_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source still matches the one the counters were taken on."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e:
+        return None
+    with open(os.path.join(ROOT, source_file), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return e["bytes_per_launch"] if e.get("source_sha256_16") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def _oracle_step(x_bits, w_bits, sm_rows, sn_rows):
+    import oracle
+    qa, sa = oracle.quantize_act_1x128(x_bits[:sm_rows])
+    qb, sb = oracle.quantize_weight_128x128(w_bits[:sn_rows])
+    oracle.gemm_block_scaled(qa, sa, qb, sb)
+    return 2.0 * sm_rows * sn_rows * K
+
+
+def _cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(x_bits, w_bits, budget_s=12.0):
+    """The oracle, untuned, on a bounded sample: X rows x W rows of the step."""
+    sm_rows, sn_rows = 512, 1024
+    flop, t0, n = 0.0, time.perf_counter(), 0
+    while True:
+        flop += _oracle_step(x_bits, w_bits, sm_rows, sn_rows)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": f"{n} x (quantize X[{sm_rows},7168] 1x128 + W[{sn_rows},7168] 128x128, "
+                      f"GEMM {sm_rows}x{sn_rows}x7168), float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from fp8_fine_grained_fp8bs_gb300 import synth
+    x_bits, w_bits = synth.dense_fprop(0)
+    ladder = [(8, 128), (32, 128), (64, 256), (128, 256), (256, 512), (512, 1024)]
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    pick = ladder[0]
+    for cand in ladder:
+        t0 = time.perf_counter()
+        _oracle_step(x_bits, w_bits, *cand)
+        if time.perf_counter() - t0 > budget:
+            break
+        pick = cand
+    for _ in range(args.warmup):
+        _oracle_step(x_bits, w_bits, *pick)
+    t0 = time.perf_counter()
+    flop = 0.0
+    for _ in range(args.steps):
+        flop += _oracle_step(x_bits, w_bits, *pick)
+    dt = time.perf_counter() - t0
+    v = flop / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_rows": list(pick)},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
+                             "sample": f"each step: quantize X[{pick[0]},7168] + W[{pick[1]},7168], "
+                                       f"GEMM {pick[0]}x{pick[1]}x7168"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="fp8bs", choices=["fp8bs", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import fp8_fine_grained_fp8bs_gb300 as fp8bs
+    from fp8_fine_grained_fp8bs_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    fp8bs.build()
+    fp8bs.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs: each rank its own batch (replica), resident in HBM before timing
+    x_bits, w_bits = synth.dense_fprop(seed=rank)
+    xin = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    win = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def step(gemm_events=None):
+        fp8bs.fp8bs_quantize_act(xin, M, K, K, xq, sx, None, None, stream)
+        fp8bs.fp8bs_quantize_weight(win, N, K, K, wq, sw, None, None, stream)
+        if gemm_events is not None:
+            gemm_events[0].record(stream)
+        fp8bs.fp8bs_gemm(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, y, fp8bs.OUT_BF16, M, N, K, 0, stream)
+        if gemm_events is not None:
+            gemm_events[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fp8bs.fp8bs_get_device_status(stream) != 0:
+        raise RuntimeError("device status after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(_gpu_id(torch, local))
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end) / args.steps)
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    gemm_ms = max_over_ranks(gemm_ms)
+    if fp8bs.fp8bs_get_device_status(stream) != 0:
+        raise RuntimeError("device status after the timed steps")
+
+    # standalone quantize of X[16384, 7168] (inputs 235 MB > L2)
+    xl_bits = synth.quantize_input(seed=rank)
+    xl = torch.from_numpy(xl_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    xlq = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
+    xls = torch.empty((QK // 128, QM), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        fp8bs.fp8bs_quantize_act(xl, QM, QK, QK, xlq, xls, None, None, stream)
+    nq = max(10, min(args.steps, 200))
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nq)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    for a, b in qev:
+        a.record(stream)
+        fp8bs.fp8bs_quantize_act(xl, QM, QK, QK, xlq, xls, None, None, stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    q_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in qev))
+    del xl, xlq, xls
+
+    # end to end through the public API with host buffers
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    w_host = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    ne = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        xin.copy_(x_host, non_blocking=True)
+        win.copy_(w_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ne):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne)
+
+    peaks, peak_src = _peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
+    q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
+    value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "out": "bf16",
+                   "quantize_shape": [QM, QK], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (X+W BF16 = 161 MB per step > 129 MB); no flush"},
+        "gemm": {"tflops": gemm_tflops, "ms": gemm_ms, "frac_of_fp8_peak": gemm_tflops / fp8_peak},
+        "quantize": {"gbs": q_gbs, "ms": q_ms, "frac_of_hbm": q_gbs / peaks["hbm_gbs"],
+                     "bytes": QUANT_BYTES},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / fp8_peak,
+                     "traffic": _traffic("gemm_dense_fprop_bf16",
+                                         "fp8_fine_grained_fp8bs_gb300/csrc/gemm.cu"),
+                     "peak_source": f"{peak_src}: bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)"},
+        "quantize_roofline": {"bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": q_gbs / peaks["hbm_gbs"],
+                              "traffic": _traffic("quantize_act_1x128_16384x7168",
+                                                  "fp8_fine_grained_fp8bs_gb300/csrc/quantize.cu"),
+                              "peak_source": peak_src},
+        "e2e": {"value": world * GEMM_FLOP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(xin.numel() * 2 + win.numel() * 2),
+                "d2h_bytes_per_step": int(y.numel() * 2), "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x_bits, w_bits)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -122,7 +122,7 @@ int fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float*
 int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets, int num_groups,
                        const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N, int64_t K, void* stream) {
   if (M_total < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
-  if (num_groups < 1 || num_groups > 1024) return FP8BS_ERR_INVALID_ARG;
+  if (num_groups < 1 || num_groups > 512) return FP8BS_ERR_INVALID_ARG;
   if (d_dtype != FP8BS_OUT_F32 && d_dtype != FP8BS_OUT_BF16) return FP8BS_ERR_INVALID_ARG;
   if (offsets == nullptr) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0 || N % 128 != 0) return FP8BS_ERR_SHAPE;

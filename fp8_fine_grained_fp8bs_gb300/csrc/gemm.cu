@@ -10,13 +10,17 @@
 //   * a persistent, warp-specialised CTA per SM: warp 0 issues TMA loads of
 //     128x128 A and BNx128 B tiles into a shared-memory ring; warp 1 issues
 //     the MMAs (4 x tcgen05.mma K=32 per 128-K block) into one of two TMEM
-//     partial buffers, the first of the four overwriting the buffer; warps
-//     4-11 (two warpgroups) fold each finished partial into FP32 registers
-//     with the block's scale (acc += P_kb * s_a * s_b) while the tensor core
-//     already computes the next block into the other buffer;
+//     partial buffers, the first of the four overwriting the buffer; warp 2
+//     copies each k-block's scales (128 row scales of A, the B scales of
+//     the tile's columns) into a shared-memory scale ring with cp.async;
+//     warps 4-11 (two warpgroups) fold each finished partial into FP32
+//     registers with the block's scales (acc += P_kb * s_a * s_b) while the
+//     tensor core computes the next block into the other buffer;
 //   * the running FP32 accumulator never leaves the registers; each thread
-//     owns one output row (its TMEM lane) and BN/2 columns;
-//   * mbarrier pipelines (smem ring full/empty, TMEM full/empty) with
+//     owns one output row (its TMEM lane) and BN/2 columns.  A TMEM buffer
+//     is released as soon as its last columns are in registers, before the
+//     last multiply-adds;
+//   * mbarrier pipelines (operand ring, scale ring, TMEM buffers) with
 //     bounded waits; a timeout records a status and unwinds.
 //
 // The same kernel serves the dense GEMM (one group) and the grouped MoE
@@ -42,7 +46,8 @@ constexpr int kEpiThreads = 256;
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 128;         // = N_C
 constexpr int kUmmaK = 32;           // K of one kind::f8f6f4 MMA (bytes of E4M3)
-constexpr int kMaxGroups = 1024;
+constexpr int kMaxGroups = 512;
+constexpr int kScaleSlots = 16;      // scale ring depth (k-blocks the loader may run ahead)
 constexpr uint32_t kTmemCols = 512;  // two partial buffers of up to 256 columns
 constexpr uint32_t kRegsProducer = 56;
 constexpr uint32_t kRegsEpilogue = 224;
@@ -52,18 +57,19 @@ struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kABytes = kBlockM * kBlockK;       // 16 KB
   static constexpr int kBBytes = BN * kBlockK;            // 16 or 32 KB
-  static constexpr int kScaleBytes = BN * 4;              // per-column B scales of one stage
+  static constexpr int kSlotFloats = kBlockM + BN;        // A row scales, then B column scales
   static constexpr int kColsPerThread = BN / 2;
   static constexpr int kChunks = kColsPerThread / 32;
   // dynamic shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffScale = kOffB + kStages * kBBytes;
-  static constexpr int kOffBar = kOffScale + kStages * kScaleBytes;
-  static constexpr int kNumBars = 4 * kStages + 4 + 1;
+  static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 4 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;       // tmem slot, abort flag, tile count
   static constexpr int kOffGroups = kOffMisc + 16;              // offsets[G+1], cum[G+1]
   static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct KParams {
@@ -84,6 +90,39 @@ struct KParams {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// acc[j] += p[j] * s for 32 accumulators, two per packed FP32x2 FMA.
+__device__ __forceinline__ void fold_block(float* acc, const uint32_t (&p)[32], float s) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    asm("{\n\t.reg .b64 a, q, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 q, {%2, %3};\n\t"
+        "mov.b64 c, {%4, %4};\n\t"
+        "fma.rn.f32x2 a, q, c, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n}"
+        : "+f"(acc[j]), "+f"(acc[j + 1])
+        : "r"(p[j]), "r"(p[j + 1]), "f"(s));
+  }
+}
+
+// acc[j] += p[j] * (s_a * s_b[j]) with per-column scales s_b (Wgrad).
+__device__ __forceinline__ void fold_row(float* acc, const uint32_t (&p)[32], float sa, const float* sb) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float2 b = *reinterpret_cast<const float2*>(sb + j);
+    asm("{\n\t.reg .b64 a, q, c, t;\n\t"
+        "mov.b64 t, {%4, %4};\n\t"
+        "mov.b64 c, {%5, %6};\n\t"
+        "mul.rn.f32x2 c, c, t;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 q, {%2, %3};\n\t"
+        "fma.rn.f32x2 a, q, c, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n}"
+        : "+f"(acc[j]), "+f"(acc[j + 1])
+        : "r"(p[j]), "r"(p[j + 1]), "f"(sa), "f"(b.x), "f"(b.y));
+  }
 }
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_status, 0, code); }
@@ -120,12 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + C::kOffB;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* full = bars;                       // [kStages] TMA -> MMA
-  uint64_t* empty = bars + C::kStages;         // [kStages] MMA -> TMA
-  uint64_t* sc_full = bars + 2 * C::kStages;   // [kStages] per-column B scales landed
-  uint64_t* sc_empty = bars + 3 * C::kStages;  // [kStages] epilogue done with them
-  uint64_t* t_full = bars + 4 * C::kStages;    // [2] partial ready in TMEM
-  uint64_t* t_empty = t_full + 2;              // [2] partial consumed
+  uint64_t* full = bars;                               // [kStages] TMA -> MMA
+  uint64_t* empty = bars + C::kStages;                 // [kStages] MMA -> TMA
+  uint64_t* sc_full = bars + 2 * C::kStages;           // [kScaleSlots] scales landed
+  uint64_t* sc_empty = sc_full + kScaleSlots;          // [kScaleSlots] epilogue done with them
+  uint64_t* t_full = sc_empty + kScaleSlots;           // [2] partial ready in TMEM
+  uint64_t* t_empty = t_full + 2;                      // [2] partial read out of TMEM
   uint64_t* teardown = t_full + 4;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* s_off = reinterpret_cast<int*>(smem + C::kOffGroups);
@@ -134,17 +173,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ntn = (p.N + BN - 1) / BN;
+  const int nnb = (p.N + kGroup - 1) / kGroup;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sc_full[s], 1);
-      mbar_init(&sc_empty[s], kEpiThreads / 32);
+    }
+    for (int s = 0; s < kScaleSlots; ++s) {
+      mbar_init(&sc_full[s], 32);                      // one cp.async arrival per loader lane
+      mbar_init(&sc_empty[s], kEpiThreads / 32);       // one arrival per epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&t_full[b], 1);
-      mbar_init(&t_empty[b], kEpiThreads);
+      mbar_init(&t_empty[b], kEpiThreads / 32);
     }
     mbar_init(teardown, 1);
     fence_barrier_init();
@@ -209,12 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0, g);
           else
             tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0);
-          if (kRowScale) {
-            if (!mbar_wait(&sc_empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
-            const int cols = min(BN, p.N - n0);
-            mbar_arrive_expect_tx(&sc_full[stage], cols * 4);
-            bulk_load(sScale + stage * BN, p.sb + static_cast<int64_t>(kb) * p.N + n0, cols * 4, &sc_full[stage]);
-          }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
@@ -262,6 +298,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait for every MMA issued so far before TMEM can be released
       mma_commit(teardown);
       (void)mbar_wait(teardown, 0, p.timeout_ns);
+    } else if (warp == 2) {
+      // ----------------------------------------------------- scale loader
+      // Slot layout: [0,128) row scales of A for the tile's 128 rows,
+      // [128, 128+BN) B scales: per column (row kind) or, for 128x128
+      // block scales, one per 128-column block of the tile.
+      int slot = 0;
+      uint32_t sph = 0;
+      bool live = true;
+      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+        int row0, n0, g;
+        tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(&sc_empty[slot], sph ^ 1, p.timeout_ns)) { live = false; break; }
+          float* dst = sScale + slot * C::kSlotFloats;
+          const float* sa_kb = p.sa + static_cast<int64_t>(kb) * p.M;
+#pragma unroll
+          for (int i = 0; i < kBlockM / 32; ++i) {
+            const int64_t r = static_cast<int64_t>(row0) + lane + 32 * i;
+            if (r < p.M) cp_async_4(dst + lane + 32 * i, sa_kb + r);
+          }
+          if (kRowScale) {
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) {
+              const int c = 4 * (lane + 32 * i);
+              if (n0 + c < p.N)
+                cp_async_16(dst + kBlockM + c, p.sb + static_cast<int64_t>(kb) * p.N + n0 + c);
+            }
+          } else if (lane < BN / 128 && n0 + 128 * lane < p.N) {
+            const int64_t nb = static_cast<int64_t>(g) * nnb + n0 / 128 + lane;
+            cp_async_4(dst + kBlockM + lane, p.sb + nb * p.nkb + kb);
+          }
+          cp_async_mbar_arrive(&sc_full[slot]);
+          if (++slot == kScaleSlots) { slot = 0; sph ^= 1; }
+        }
+      }
+      if (!live) {
+        record_status(kStatusTimeout);
+        *abort_flag = 1;
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else {
     setmaxnreg_inc<kRegsEpilogue>();
@@ -269,65 +345,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = warp - kEpiWarp0;      // 0..7
     const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
     const int colhalf = e >> 2;          // which BN/2 columns
+    const int row_in_tile = quarter * 32 + lane;
     uint32_t buf = 0, tphase = 0;
-    int sstage = 0;
-    uint32_t sphase = 0;
+    int slot = 0;
+    uint32_t sph = 0;
     bool live = true;
     for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
       int row0, n0, g;
       tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
-      const int64_t m = static_cast<int64_t>(row0) + quarter * 32 + lane;
+      const int64_t m = static_cast<int64_t>(row0) + row_in_tile;
       const bool mvalid = m < p.M;
       const int ncol0 = n0 + colhalf * C::kColsPerThread;
-      const float* sbp = nullptr;
-      if (!kRowScale)
-        sbp = p.sb + (static_cast<int64_t>(g) * ((p.N + kGroup - 1) / kGroup) + ncol0 / kGroup) * p.nkb;
+      const int bsel = (colhalf * C::kColsPerThread) / 128;   // which 128-column block of the tile
       float acc[C::kColsPerThread];
 #pragma unroll
       for (int j = 0; j < C::kColsPerThread; ++j) acc[j] = 0.0f;
-      float sa_next = mvalid ? __ldg(p.sa + m) : 0.0f;
-      float sb_next = (!kRowScale && ncol0 < p.N) ? __ldg(sbp) : 0.0f;
       for (int kb = 0; kb < p.nkb; ++kb) {
-        const float sa_cur = sa_next;
-        const float sb_cur = sb_next;
-        if (kb + 1 < p.nkb) {
-          sa_next = mvalid ? __ldg(p.sa + static_cast<int64_t>(kb + 1) * p.M + m) : 0.0f;
-          if (!kRowScale && ncol0 < p.N) sb_next = __ldg(sbp + kb + 1);
-        }
+        if (!mbar_wait(&sc_full[slot], sph, p.timeout_ns)) { live = false; break; }
         if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
-        if (kRowScale && !mbar_wait(&sc_full[sstage], sphase, p.timeout_ns)) { live = false; break; }
         tc_fence_after_sync();
+        const float* scs = sScale + slot * C::kSlotFloats;
+        const float sa = scs[row_in_tile];
+        const float s_ab = kRowScale ? sa : sa * scs[kBlockM + bsel];
+        const float* scol = scs + kBlockM + colhalf * C::kColsPerThread;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                colhalf * C::kColsPerThread;
-        const float s_ab = sa_cur * sb_cur;
+        // TMEM -> registers 64 columns per round; the buffer is handed back
+        // to the MMA as soon as the last round has landed.
 #pragma unroll
-        for (int ch = 0; ch < C::kChunks; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(taddr + ch * 32, r);
-          tmem_wait_ld(r);
+        for (int ch = 0; ch < C::kChunks; ch += 2) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + ch * 32, ra);
+          tmem_ld32(taddr + (ch + 1) * 32, rb);
+          tmem_wait_ld(ra);
+          tmem_wait_ld(rb);
+          if (ch + 2 == C::kChunks) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&t_empty[buf]);
+          }
           if (kRowScale) {
-            const float4* sc4 = reinterpret_cast<const float4*>(sScale + sstage * BN + colhalf * C::kColsPerThread +
-                                                                ch * 32);
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 sc = sc4[j4];
-              acc[ch * 32 + 4 * j4 + 0] = fmaf(__uint_as_float(r[4 * j4 + 0]), sa_cur * sc.x, acc[ch * 32 + 4 * j4 + 0]);
-              acc[ch * 32 + 4 * j4 + 1] = fmaf(__uint_as_float(r[4 * j4 + 1]), sa_cur * sc.y, acc[ch * 32 + 4 * j4 + 1]);
-              acc[ch * 32 + 4 * j4 + 2] = fmaf(__uint_as_float(r[4 * j4 + 2]), sa_cur * sc.z, acc[ch * 32 + 4 * j4 + 2]);
-              acc[ch * 32 + 4 * j4 + 3] = fmaf(__uint_as_float(r[4 * j4 + 3]), sa_cur * sc.w, acc[ch * 32 + 4 * j4 + 3]);
-            }
+            fold_row(acc + ch * 32, ra, s_ab, scol + ch * 32);
+            fold_row(acc + (ch + 1) * 32, rb, s_ab, scol + (ch + 1) * 32);
           } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), s_ab, acc[ch * 32 + j]);
+            fold_block(acc + ch * 32, ra, s_ab);
+            fold_block(acc + (ch + 1) * 32, rb, s_ab);
           }
         }
-        tc_fence_before_sync();
-        mbar_arrive(&t_empty[buf]);
-        if (kRowScale) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sc_empty[sstage]);
-          if (++sstage == C::kStages) { sstage = 0; sphase ^= 1; }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc_empty[slot]);
+        if (++slot == kScaleSlots) { slot = 0; sph ^= 1; }
         buf ^= 1;
         if (buf == 0) tphase ^= 1;
       }

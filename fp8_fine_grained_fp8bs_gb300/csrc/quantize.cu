@@ -4,9 +4,10 @@
 // "online quantization"; formulas of the Figure 7 explainer: for each group
 // s = absmax / 448 and code = round(x / s).  Exactly as the C ABI states:
 // s = fl32(absmax / 448) and code = E4M3_rne_satfinite(fl32(x / s)), both
-// divisions IEEE round-to-nearest (__fdiv_rn); a group with s == 0 gets
-// all-zero codes.  The kernels are HBM-bound streaming kernels: every byte
-// is read once and written once, with coalesced 16-byte loads.
+// quotients IEEE round-to-nearest; a group with s == 0 gets all-zero codes.
+// The per-element quotient is decided from a two-sided bracket of x * (1/s)
+// (quant2 below), so the kernels stay HBM-bound streaming kernels: every
+// byte is read once and written once, with coalesced 16-byte loads.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -23,10 +24,71 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Quotient x / s rounded once to float32, then to E4M3; s == 0 gives code 0.
-__device__ __forceinline__ uint32_t quant2(float a, float b, float s) {
+// Per-group divisor s and a bracket [r_lo, r_hi] of 1/s (both float32).
+struct Divisor {
+  float s;
+  float r_lo, r_hi;
+  bool fast;  // s is a normal float32; s == 0 and subnormal s take the exact path
+};
+
+__device__ __forceinline__ Divisor make_divisor(float absmax) {
+  Divisor d;
+  d.s = __fdiv_rn(absmax, kE4M3Max);  // s = fl32(absmax / 448)
+  d.fast = d.s >= 1.17549435e-38f;    // FLT_MIN: 1/s is then a finite normal float
+  const float s = d.fast ? d.s : 1.0f;
+  d.r_lo = __frcp_rd(s);              // r_lo <= 1/s
+  // r_hi >= 1/s: r_lo itself when 1/s is exact (r_lo * s == 1, tested
+  // exactly by one fused multiply-add), else the next float up.
+  d.r_hi = (fmaf(d.r_lo, s, -1.0f) == 0.0f) ? d.r_lo : __uint_as_float(__float_as_uint(d.r_lo) + 1u);
+  return d;
+}
+
+// E4M3 codes of fl32(x0 / s) and fl32(x1 / s) for the two BF16 values of
+// `w` (x0 in the low half), without a division per element:
+//   lo = RD(|x| * r_lo) <= |x| / s <= RU(|x| * r_hi) = hi,
+// so the correctly rounded quotient fl32(|x| / s) lies in [lo, hi] too.
+// Rounding to E4M3 (RNE, saturating) is monotonic, hence when lo and hi
+// round to the same codes, so does fl32(|x| / s).  When an E4M3 rounding
+// boundary falls inside the 2-3 ulp wide bracket (rare), or s is not a
+// normal float, `bad` is set and the caller redoes the chunk with IEEE
+// divisions (quant8_exact).  The sign is applied last: the quotient has
+// x's sign, also for -0 and for results that round to zero.
+__device__ __forceinline__ uint32_t quant2(uint32_t w, const Divisor& d, bool& bad) {
+  const float a0 = fabsf(bf16_lo(w)), a1 = fabsf(bf16_hi(w));
+  const uint32_t c = e4m3x2(__fmul_rd(a0, d.r_lo), __fmul_rd(a1, d.r_lo));
+  const uint32_t c_hi = e4m3x2(__fmul_ru(a0, d.r_hi), __fmul_ru(a1, d.r_hi));
+  bad |= (c != c_hi);
+  return d.s == 0.0f ? 0u : (c | ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u));
+}
+
+__device__ __forceinline__ float absmax8(uint4 v) {
+  const float m0 = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
+  const float m1 = fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)));
+  const float m2 = fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z)));
+  const float m3 = fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)));
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// Eight consecutive values -> eight codes (byte i = value i).
+__device__ __forceinline__ uint2 quant8(uint4 v, const Divisor& d, bool& bad) {
+  bad |= !d.fast;
+  return make_uint2(quant2(v.x, d, bad) | (quant2(v.y, d, bad) << 16),
+                    quant2(v.z, d, bad) | (quant2(v.w, d, bad) << 16));
+}
+
+// The same codes through IEEE divisions, x / s then E4M3 (the fix-up path).
+__device__ __forceinline__ uint32_t quant1_exact(uint32_t h, float s) {
   if (s == 0.0f) return 0u;
-  return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+  const float q = __fdiv_rn(__uint_as_float(h << 16), s);
+  return e4m3x2(q, 0.0f) & 0xFFu;
+}
+
+__device__ __forceinline__ uint2 quant8_exact(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = quant1_exact((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu), s);
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
 __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
@@ -38,55 +100,102 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
-// 1x128 tiles.  A half-warp owns one group (16 lanes x 8 BF16 = 128 values,
-// 256 contiguous bytes); a warp owns two consecutive groups of the
-// row-major (row, kb) enumeration, so consecutive warps stream consecutive
-// memory.  Each thread keeps kUnroll independent 16-byte loads in flight.
+// 1x128 tiles.  Eight lanes own one group: lane l holds elements 8l..8l+7
+// and 64+8l..64+8l+7 (two 16-byte loads, each warp-wide load instruction
+// covering four contiguous 128-byte segments); a warp owns four consecutive
+// groups of the row-major (row, kb) enumeration, so consecutive warps stream
+// consecutive memory.  Each thread keeps 2*kUnroll 16-byte loads in flight.
 template <int kUnroll>
 __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M,
                                                                int nkb, int64_t ldx, uint8_t* __restrict__ xq,
                                                                float* __restrict__ sx) {
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int hl = lane & 15;
+  const int sub = lane >> 3;
+  const int gl = lane & 7;
   const int64_t K = static_cast<int64_t>(nkb) * kGroup;
   const int64_t units = M * nkb;
-  const int64_t pairs = (units + 1) >> 1;
+  const int64_t quads = (units + 3) >> 2;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
 
-  for (int64_t p0 = warp0; p0 < pairs; p0 += nwarps * kUnroll) {
-    uint4 v[kUnroll];
+  for (int64_t q0 = warp0; q0 < quads; q0 += nwarps * kUnroll) {
+    uint4 v0[kUnroll], v1[kUnroll];
     int64_t m[kUnroll], kb[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int i = 0; i < kUnroll; ++i) {
-      const int64_t u = 2 * (p0 + i * nwarps) + half;
+      const int64_t u = 4 * (q0 + i * nwarps) + sub;
       ok[i] = u < units;
       m[i] = ok[i] ? u / nkb : 0;
       kb[i] = ok[i] ? u - m[i] * nkb : 0;
-      v[i] = ok[i] ? ld_stream_16(x + m[i] * ldx + kb[i] * kGroup + hl * 8) : make_uint4(0, 0, 0, 0);
+      const uint16_t* p = x + m[i] * ldx + kb[i] * kGroup + gl * 8;
+      v0[i] = ok[i] ? ld_stream_16(p) : make_uint4(0, 0, 0, 0);
+      v1[i] = ok[i] ? ld_stream_16(p + 64) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kUnroll; ++i) {
-      const float f0 = bf16_lo(v[i].x), f1 = bf16_hi(v[i].x), f2 = bf16_lo(v[i].y), f3 = bf16_hi(v[i].y);
-      const float f4 = bf16_lo(v[i].z), f5 = bf16_hi(v[i].z), f6 = bf16_lo(v[i].w), f7 = bf16_hi(v[i].w);
-      float a = fmaxf(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))),
-                      fmaxf(fmaxf(fabsf(f4), fabsf(f5)), fmaxf(fabsf(f6), fabsf(f7))));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+      float a = fmaxf(absmax8(v0[i]), absmax8(v1[i]));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      const float s = __fdiv_rn(a, kE4M3Max);
-      uint2 q;
-      q.x = quant2(f0, f1, s) | (quant2(f2, f3, s) << 16);
-      q.y = quant2(f4, f5, s) | (quant2(f6, f7, s) << 16);
+      const Divisor d = make_divisor(a);
+      bool bad0 = false, bad1 = false;
+      uint2 q0v = quant8(v0[i], d, bad0);
+      uint2 q1v = quant8(v1[i], d, bad1);
+      if (bad0) q0v = quant8_exact(v0[i], d.s);
+      if (bad1) q1v = quant8_exact(v1[i], d.s);
       if (ok[i]) {
-        *reinterpret_cast<uint2*>(xq + m[i] * K + kb[i] * kGroup + hl * 8) = q;
-        if (hl == 0) sx[kb[i] * M + m[i]] = s;
+        uint8_t* o = xq + m[i] * K + kb[i] * kGroup + gl * 8;
+        *reinterpret_cast<uint2*>(o) = q0v;
+        *reinterpret_cast<uint2*>(o + 64) = q1v;
+        if (gl == 0) sx[kb[i] * M + m[i]] = d.s;
       }
     }
   }
+}
+
+// BF16 bits of column i (0..7) of an 8-value row chunk.
+__device__ __forceinline__ uint32_t col16(const uint4& v, int i) {
+  const uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
+  return (i & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// Codes of column i of rows 0..7 (one byte per row, row 0 lowest).
+__device__ __forceinline__ uint2 quant_col8(const uint4 (&v)[8], int i, const Divisor& d, bool& bad) {
+  bad |= !d.fast;
+  uint32_t p[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) p[j] = quant2(col16(v[2 * j], i) | (col16(v[2 * j + 1], i) << 16), d, bad);
+  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
+// the result is byte i of row j.
+__device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
+  const int wsel = i >> 2;
+  const uint32_t b = static_cast<uint32_t>(i & 3);
+  const uint32_t sel = b | ((b + 4) << 4);  // byte b of the first word, byte b of the second
+  uint32_t p[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x0 = wsel ? q[2 * j].y : q[2 * j].x;
+    const uint32_t x1 = wsel ? q[2 * j + 1].y : q[2 * j + 1].x;
+    p[j] = __byte_perm(x0, x1, sel);
+  }
+  return make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
+}
+
+// Exact fix-up of one 8-row column chunk, re-reading the BF16 inputs.
+__device__ __noinline__ uint2 quant_col8_exact(const uint16_t* x, int64_t ld, float s) {
+  uint32_t b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = quant1_exact(x[j * ld], s);
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Exact fix-up of one 8-value row chunk, re-reading the BF16 inputs.
+__device__ __noinline__ uint2 quant_row8_exact(const uint16_t* x, float s) {
+  return quant8_exact(*reinterpret_cast<const uint4*>(x), s);
 }
 
 // ---------------------------------------------------------------------------
@@ -111,30 +220,25 @@ __global__ void __launch_bounds__(256) quant_act_dual_kernel(const uint16_t* __r
   const int64_t r0 = rb * kGroup + 8 * g;
   const int64_t c0 = kb * kGroup + 8 * c;
 
-  float f[8][8];
+  uint4 v[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint4 v = ld_stream_16(x + (r0 + j) * ldx + c0);
-    f[j][0] = bf16_lo(v.x); f[j][1] = bf16_hi(v.x); f[j][2] = bf16_lo(v.y); f[j][3] = bf16_hi(v.y);
-    f[j][4] = bf16_lo(v.z); f[j][5] = bf16_hi(v.z); f[j][6] = bf16_lo(v.w); f[j][7] = bf16_hi(v.w);
-  }
+  for (int j = 0; j < 8; ++j) v[j] = ld_stream_16(x + (r0 + j) * ldx + c0);
 
   // 1x128 groups: one per row.
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[j][i]));
+    float a = absmax8(v[j]);
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    const float s = __fdiv_rn(a, kE4M3Max);
-    uint2 q;
-    q.x = quant2(f[j][0], f[j][1], s) | (quant2(f[j][2], f[j][3], s) << 16);
-    q.y = quant2(f[j][4], f[j][5], s) | (quant2(f[j][6], f[j][7], s) << 16);
-    *reinterpret_cast<uint2*>(xq + (r0 + j) * K + c0) = q;
-    if (c == 0) sx[kb * M + r0 + j] = s;
+    const Divisor d = make_divisor(a);
+    bool bad = false;
+    const uint2 q = quant8(v[j], d, bad);
+    uint8_t* o = xq + (r0 + j) * K + c0;
+    *reinterpret_cast<uint2*>(o) = q;
+    if (bad) *reinterpret_cast<uint2*>(o) = quant_row8_exact(x + (r0 + j) * ldx + c0, d.s);
+    if (c == 0) sx[kb * M + r0 + j] = d.s;
   }
 
   // 128x1 groups: one per column.
@@ -142,7 +246,7 @@ __global__ void __launch_bounds__(256) quant_act_dual_kernel(const uint16_t* __r
   for (int i = 0; i < 8; ++i) {
     float a = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j][i]));
+    for (int j = 0; j < 8; ++j) a = fmaxf(a, __uint_as_float((col16(v[j], i) & 0x7FFFu) << 16));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
     if ((t & 16) == 0) red[warp][8 * c + i] = a;
   }
@@ -151,18 +255,18 @@ __global__ void __launch_bounds__(256) quant_act_dual_kernel(const uint16_t* __r
     float a = red[0][t];
 #pragma unroll
     for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
-    const float s = __fdiv_rn(a, kE4M3Max);
-    scol[t] = s;
-    sx_t[rb * K + kb * kGroup + t] = s;
+    scol[t] = a;
+    sx_t[rb * K + kb * kGroup + t] = __fdiv_rn(a, kE4M3Max);
   }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float s = scol[8 * c + i];
-    uint2 q;
-    q.x = quant2(f[0][i], f[1][i], s) | (quant2(f[2][i], f[3][i], s) << 16);
-    q.y = quant2(f[4][i], f[5][i], s) | (quant2(f[6][i], f[7][i], s) << 16);
-    *reinterpret_cast<uint2*>(xq_t + (c0 + i) * M + r0) = q;
+    const Divisor d = make_divisor(scol[8 * c + i]);
+    bool bad = false;
+    const uint2 q = quant_col8(v, i, d, bad);
+    uint8_t* o = xq_t + (c0 + i) * M + r0;
+    *reinterpret_cast<uint2*>(o) = q;
+    if (bad) *reinterpret_cast<uint2*>(o) = quant_col8_exact(x + r0 * ldx + c0 + i, ldx, d.s);
   }
 }
 
@@ -185,16 +289,12 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
   const int64_t r0 = nb * kGroup + 8 * g;
   const int64_t c0 = kb * kGroup + 8 * c;
 
-  float f[8][8];
+  uint4 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = ld_stream_16(w + (r0 + j) * ldw + c0);
   float a = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint4 v = ld_stream_16(w + (r0 + j) * ldw + c0);
-    f[j][0] = bf16_lo(v.x); f[j][1] = bf16_hi(v.x); f[j][2] = bf16_lo(v.y); f[j][3] = bf16_hi(v.y);
-    f[j][4] = bf16_lo(v.z); f[j][5] = bf16_hi(v.z); f[j][6] = bf16_lo(v.w); f[j][7] = bf16_hi(v.w);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[j][i]));
-  }
+  for (int j = 0; j < 8; ++j) a = fmaxf(a, absmax8(v[j]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   if ((t & 31) == 0) red[t >> 5] = a;
@@ -202,26 +302,31 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
   a = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-  const float s = __fdiv_rn(a, kE4M3Max);
+  const Divisor d = make_divisor(a);
   if (t == 0) {
-    sw[nb * nkb + kb] = s;
-    if (sw_t != nullptr) sw_t[kb * nnb + nb] = s;
+    sw[nb * nkb + kb] = d.s;
+    if (sw_t != nullptr) sw_t[kb * nnb + nb] = d.s;
   }
+  uint2 q[8];
+  uint32_t bad_rows = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint2 q;
-    q.x = quant2(f[j][0], f[j][1], s) | (quant2(f[j][2], f[j][3], s) << 16);
-    q.y = quant2(f[j][4], f[j][5], s) | (quant2(f[j][6], f[j][7], s) << 16);
-    *reinterpret_cast<uint2*>(wq + (r0 + j) * K + c0) = q;
+    bool bad = false;
+    q[j] = quant8(v[j], d, bad);
+    bad_rows |= bad ? (1u << j) : 0u;
   }
-  if (wq_t != nullptr) {
+  if (bad_rows) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint2 q;
-      q.x = quant2(f[0][i], f[1][i], s) | (quant2(f[2][i], f[3][i], s) << 16);
-      q.y = quant2(f[4][i], f[5][i], s) | (quant2(f[6][i], f[7][i], s) << 16);
-      *reinterpret_cast<uint2*>(wq_t + (c0 + i) * N + r0) = q;
-    }
+    for (int j = 0; j < 8; ++j)
+      if (bad_rows & (1u << j)) q[j] = quant_row8_exact(w + (r0 + j) * ldw + c0, d.s);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(wq + (r0 + j) * K + c0) = q[j];
+  if (wq_t != nullptr) {
+    // One scale for the whole block, so the codes of W^T are the transposed
+    // codes of W: transpose this thread's 8x8 byte tile in registers.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(wq_t + (c0 + i) * N + r0) = byte_column(q, i);
   }
 }
 
@@ -229,10 +334,10 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
 
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
                                       float* sx, int sm_count, cudaStream_t stream) {
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 2;
   const int nkb = static_cast<int>(K / kGroup);
-  const int64_t pairs = (M * nkb + 1) / 2;
-  const int64_t warps_needed = (pairs + kUnroll - 1) / kUnroll;
+  const int64_t quads = (M * nkb + 3) / 4;
+  const int64_t warps_needed = (quads + kUnroll - 1) / kUnroll;
   const int64_t blocks_needed = (warps_needed + 7) / 8;
   const int64_t max_blocks = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM
   const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);

@@ -144,7 +144,7 @@ int fp8bs_gemm(const uint8_t* a, const float* sa,
  *            FP8BS_ERR_DEVICE_ARG.
  *   b        [num_groups][N][K] E4M3.  sb [num_groups][N/128][K/128].
  *   d        [M_total][N] FP32 or BF16; rows outside every group are not written.
- * Rules: K % 128 == 0, N % 128 == 0, 1 <= num_groups <= 1024.
+ * Rules: K % 128 == 0, N % 128 == 0, 1 <= num_groups <= 512.
  */
 int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total,
                        const int32_t* offsets, int num_groups,

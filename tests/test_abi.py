@@ -85,7 +85,7 @@ def test_gemm_argument_errors(lib):
 def test_grouped_gemm_argument_errors(lib):
     g = lib.fp8bs_grouped_gemm
     assert g(FAKE, FAKE, 256, FAKE, 0, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # no groups
-    assert g(FAKE, FAKE, 256, FAKE, 1025, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1
+    assert g(FAKE, FAKE, 256, FAKE, 513, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1
     assert g(FAKE, FAKE, 256, None, 2, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # offsets missing
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE, 0, 128, 100, None) == 2
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
