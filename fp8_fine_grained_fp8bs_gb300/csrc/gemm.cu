@@ -52,11 +52,13 @@ constexpr uint32_t kTmemCols = 512;  // two partial buffers of up to 256 columns
 constexpr uint32_t kRegsProducer = 56;
 constexpr uint32_t kRegsEpilogue = 224;
 
-template <int BN>
+// BN is the tile width of one CTA's output; with kPair (2-SM MMA) each CTA
+// holds only half of the B tile's rows in its shared memory.
+template <int BN, bool kPair>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kABytes = kBlockM * kBlockK;       // 16 KB
-  static constexpr int kBBytes = BN * kBlockK;            // 16 or 32 KB
+  static constexpr int kABytes = kBlockM * kBlockK;                   // 16 KB
+  static constexpr int kBBytes = (kPair ? BN / 2 : BN) * kBlockK;     // 16 or 32 KB per CTA
+  static constexpr int kStages = (kABytes + kBBytes) == 48 * 1024 ? 4 : 6;
   static constexpr int kSlotFloats = kBlockM + BN;        // A row scales, then B column scales
   static constexpr int kColsPerThread = BN / 2;
   static constexpr int kChunks = kColsPerThread / 32;
@@ -65,7 +67,7 @@ struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffScale = kOffB + kStages * kBBytes;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
-  static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 4 + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 4 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;       // tmem slot, abort flag, tile count
   static constexpr int kOffGroups = kOffMisc + 16;              // offsets[G+1], cum[G+1]
   static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
@@ -130,11 +132,22 @@ __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_stat
 // Tile t -> (first row, first column, group).  Tiles run m-tile-major with
 // the BN-wide n-tiles of one m-tile consecutive, so concurrently running
 // CTAs share A rows.
-template <int BN>
+//
+// With CTA pairs (a cluster of two running one 2-SM MMA over a 256-row
+// tile), work unit t names an (m-tile pair, n-tile); the CTA of rank r
+// takes m-tile 2*(pair) + r.
+//
+// Every role walks the k-blocks of work unit t starting at t % (K/128) and
+// wrapping around: CTAs that share an A or B tile then read different
+// k-slices of it at any moment instead of all hitting the same lines.  The
+// blocks are summed in that order (the sum is the same up to FP32 rounding
+// order).
+template <int BN, bool kPair>
 __device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const int* s_off, const int* s_cum,
-                                            int num_groups, int& row0, int& n0, int& g) {
-  const int mt = t / ntn;
-  n0 = (t - mt * ntn) * BN;
+                                            int num_groups, uint32_t rank, int& row0, int& n0, int& g) {
+  const int mu = t / ntn;
+  const int mt = kPair ? 2 * mu + static_cast<int>(rank) : mu;
+  n0 = (t - mu * ntn) * BN;
   if (!grouped) {
     g = 0;
     row0 = mt * kBlockM;
@@ -149,10 +162,10 @@ __device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const 
   row0 = s_off[g] + (mt - s_cum[g]) * kBlockM;
 }
 
-template <int BN, bool kRowScale, bool kGrouped>
+template <int BN, bool kRowScale, bool kGrouped, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem + C::kOffA;
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sc_empty = sc_full + kScaleSlots;          // [kScaleSlots] epilogue done with them
   uint64_t* t_full = sc_empty + kScaleSlots;           // [2] partial ready in TMEM
   uint64_t* t_empty = t_full + 2;                      // [2] partial read out of TMEM
-  uint64_t* teardown = t_full + 4;
+  uint64_t* teardown = t_full + 4;                     // [2] one per MMA issuer
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* s_off = reinterpret_cast<int*>(smem + C::kOffGroups);
   int* s_cum = s_off + (kMaxGroups + 1);
@@ -173,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ntn = (p.N + BN - 1) / BN;
+  // work units are tiles, or tile pairs handled by the two CTAs of a cluster
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int unit0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int nunits = kPair ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
   const int nnb = (p.N + kGroup - 1) / kGroup;
 
   if (threadIdx.x == 0) {
@@ -186,9 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&t_full[b], 1);
-      mbar_init(&t_empty[b], kEpiThreads / 32);
+      mbar_init(&t_empty[b], (kPair ? 2 : 1) * kEpiThreads / 32);  // with pairs: both CTAs' epilogue warps
     }
-    mbar_init(teardown, 1);
+    mbar_init(&teardown[0], 1);
+    mbar_init(&teardown[1], 1);
     fence_barrier_init();
     // tile count (and, for the grouped GEMM, the validated group table)
     int total_mt = 0;
@@ -214,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       total_mt = static_cast<int>((p.M + kBlockM - 1) / kBlockM);
     }
+    if (kPair) total_mt = (total_mt + 1) / 2;
     misc[1] = 0;  // abort flag
     misc[2] = static_cast<uint32_t>(total_mt * ntn);
   }
@@ -222,12 +241,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&misc[0], kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&misc[0], kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&misc[0], kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (kPair) cluster_sync();  // the peer's barriers exist before anything signals them
   const uint32_t tmem_base = misc[0];
   const int total_tiles = static_cast<int>(misc[2]);
   volatile uint32_t* abort_flag = &misc[1];
@@ -240,11 +265,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool live = true;
       int issued = 0;
-      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+      for (int t = unit0; t < total_tiles && live; t += nunits) {
         int row0, n0, g;
-        tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
+        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
+          if (kPair) {
+            // Both CTAs' tiles complete on the leader's barrier, which the
+            // leader arms for the pair's bytes; each CTA loads its A rows
+            // and its half of the B tile into its own shared memory.
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (C::kABytes + C::kBBytes));
+            const uint32_t leader_full = mapa_shared(&full[stage], 0);
+            tma_load_2d_pair(sA + stage * C::kABytes, &tmA, leader_full, kb * kBlockK, row0);
+            tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
+                             n0 + static_cast<int>(rank) * (BN / 2));
+            ++issued;
+            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            continue;
+          }
           mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
           tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBlockK, row0);
           if (kGrouped)
@@ -259,45 +297,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_status(kStatusTimeout);
         *abort_flag = 1;
         // let the copies already issued land before the CTA can exit
-        for (int s = 0; s < C::kStages && s < issued; ++s) {
+        for (int s = 0; s < C::kStages && s < issued && (!kPair || rank == 0); ++s) {
           int st = stage - 1 - s;
           uint32_t ph = phase;
           if (st < 0) { st += C::kStages; ph ^= 1; }
           (void)mbar_wait(&full[st], ph, p.timeout_ns);
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // --------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t buf = 0, tphase = 0;
+    } else if ((warp == 1 || warp == 3) && lane == 0 && rank == 0) {
+      // --------------------------------------------------------- MMA issuers
+      // Two issuing threads on different SM sub-partitions take alternate
+      // k-block steps (warp 1 the even ones, warp 3 the odd ones), so each
+      // owns one TMEM buffer.  Issuing MMAs holds up tcgen05.ld on the
+      // issuer's sub-partition; splitting the issue halves that stall for
+      // the epilogue warps that share it.  With pairs only the leader CTA
+      // issues: one M=256 MMA covers both CTAs.
+      constexpr uint32_t idesc = idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, BN);
+      const uint32_t parity = warp == 1 ? 0u : 1u;
+      const uint32_t buf = parity;
+      uint32_t step = 0;
       bool live = true;
-      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
-        for (int kb = 0; kb < p.nkb; ++kb) {
+      for (int t = unit0; t < total_tiles && live; t += nunits) {
+        for (int kk = 0; kk < p.nkb; ++kk, ++step) {
+          if ((step & 1u) != parity) continue;
+          const int stage = static_cast<int>(step % C::kStages);
+          const uint32_t phase = (step / C::kStages) & 1u;
+          const uint32_t tphase = (step >> 1) & 1u;
           if (!mbar_wait(&full[stage], phase, p.timeout_ns)) { live = false; break; }
           if (!mbar_wait(&t_empty[buf], tphase ^ 1, p.timeout_ns)) { live = false; break; }
           tc_fence_after_sync();
           const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
           const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
           const uint32_t dtmem = tmem_base + buf * BN;
+          if (kPair) {
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k)
-            mma_e4m3(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-          mma_commit(&empty[stage]);
-          mma_commit(&t_full[buf]);
-          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-          buf ^= 1;
-          if (buf == 0) tphase ^= 1;
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              mma_e4m3_pair(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+            mma_commit_pair(&empty[stage], 0x3);
+            mma_commit_pair(&t_full[buf], 0x3);
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              mma_e4m3(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+            mma_commit(&empty[stage]);
+            mma_commit(&t_full[buf]);
+          }
         }
       }
       if (!live) {
         record_status(kStatusTimeout);
         *abort_flag = 1;
       }
-      // wait for every MMA issued so far before TMEM can be released
-      mma_commit(teardown);
-      (void)mbar_wait(teardown, 0, p.timeout_ns);
+      // wait for every MMA this thread issued before TMEM can be released
+      if (kPair)
+        mma_commit_pair(&teardown[parity], 0x1);
+      else
+        mma_commit(&teardown[parity]);
+      (void)mbar_wait(&teardown[parity], 0, p.timeout_ns);
     } else if (warp == 2) {
       // ----------------------------------------------------- scale loader
       // Slot layout: [0,128) row scales of A for the tile's 128 rows,
@@ -306,10 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0;
       uint32_t sph = 0;
       bool live = true;
-      for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+      for (int t = unit0; t < total_tiles && live; t += nunits) {
         int row0, n0, g;
-        tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
+        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
           if (!mbar_wait(&sc_empty[slot], sph ^ 1, p.timeout_ns)) { live = false; break; }
           float* dst = sScale + slot * C::kSlotFloats;
           const float* sa_kb = p.sa + static_cast<int64_t>(kb) * p.M;
@@ -350,9 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int slot = 0;
     uint32_t sph = 0;
     bool live = true;
-    for (int t = blockIdx.x; t < total_tiles && live; t += gridDim.x) {
+    for (int t = unit0; t < total_tiles && live; t += nunits) {
       int row0, n0, g;
-      tile_coords<BN>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, row0, n0, g);
+      tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
       const int64_t m = static_cast<int64_t>(row0) + row_in_tile;
       const bool mvalid = m < p.M;
       const int ncol0 = n0 + colhalf * C::kColsPerThread;
@@ -360,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[C::kColsPerThread];
 #pragma unroll
       for (int j = 0; j < C::kColsPerThread; ++j) acc[j] = 0.0f;
-      for (int kb = 0; kb < p.nkb; ++kb) {
+      for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
         if (!mbar_wait(&sc_full[slot], sph, p.timeout_ns)) { live = false; break; }
         if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
         tc_fence_after_sync();
@@ -382,7 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ch + 2 == C::kChunks) {
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&t_empty[buf]);
+            if (lane == 0) {
+              if (kPair)
+                mbar_arrive_cluster(mapa_shared(&t_empty[buf], 0));  // the leader's MMA waits on it
+              else
+                mbar_arrive(&t_empty[buf]);
+            }
           }
           if (kRowScale) {
             fold_row(acc + ch * 32, ra, s_ab, scol + ch * 32);
@@ -435,7 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (kPair) cluster_sync();  // no CTA leaves while its peer may still signal or use it
+  if (warp == 1) {
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // --------------------------------------------------------------- host side
@@ -473,10 +540,10 @@ bool encode_operand(CUtensorMap* map, const void* base, int rank, const uint64_t
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool kRowScale, bool kGrouped>
+template <int BN, bool kRowScale, bool kGrouped, bool kPair>
 cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap_failed, bool* reg_check_failed) {
-  using C = Cfg<BN>;
-  auto kern = gemm_kernel<BN, kRowScale, kGrouped>;
+  using C = Cfg<BN, kPair>;
+  auto kern = gemm_kernel<BN, kRowScale, kGrouped, kPair>;
   // The register split (warps 0-3 shrink to kRegsProducer, warps 4-11 grow
   // to kRegsEpilogue) must fit in what the CTA is launched with.
   cudaFuncAttributes attr;
@@ -494,15 +561,16 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
   const uint64_t dA[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
   const uint64_t sA[1] = {static_cast<uint64_t>(a.K)};
   if (!encode_operand(&tmA, a.a, 2, dA, sA, kBlockM)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+  const uint32_t b_rows = kPair ? BN / 2 : BN;  // with pairs each CTA fetches half of the B tile
   if (kGrouped) {
     const uint64_t dB[3] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N),
                             static_cast<uint64_t>(a.num_groups)};
     const uint64_t sB[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.K) * a.N};
-    if (!encode_operand(&tmB, a.b, 3, dB, sB, BN)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+    if (!encode_operand(&tmB, a.b, 3, dB, sB, b_rows)) { *tmap_failed = true; return cudaErrorInvalidValue; }
   } else {
     const uint64_t dB[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.N)};
     const uint64_t sB[1] = {static_cast<uint64_t>(a.K)};
-    if (!encode_operand(&tmB, a.b, 2, dB, sB, BN)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+    if (!encode_operand(&tmB, a.b, 2, dB, sB, b_rows)) { *tmap_failed = true; return cudaErrorInvalidValue; }
   }
 
   KParams kp;
@@ -518,14 +586,41 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
   kp.accumulate = a.accumulate ? 1 : 0;
   kp.timeout_ns = a.timeout_ns;
 
-  // Persistent grid: one CTA per SM, or fewer when there are fewer tiles.
-  // (The grouped tile count lives on the device; the grid covers its bound.)
+  // Persistent grid: one CTA per SM (one cluster per SM pair), or fewer
+  // when there are fewer work units.  (The grouped tile count lives on the
+  // device; the grid covers its bound.)
   const int64_t ntn = (a.N + BN - 1) / BN;
-  const int64_t mt_bound = kGrouped ? (a.M / kBlockM + a.num_groups) : (a.M + kBlockM - 1) / kBlockM;
-  const int64_t tiles = mt_bound * ntn;
-  const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
-  if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, kp);
+  int64_t mt_bound = kGrouped ? (a.M / kBlockM + a.num_groups) : (a.M + kBlockM - 1) / kBlockM;
+  if (kPair) mt_bound = (mt_bound + 1) / 2;
+  const int64_t units = mt_bound * ntn;
+  if (units <= 0) return cudaSuccess;
+  if (!kPair) {
+    const int grid = static_cast<int>(std::min<int64_t>(units, sm_count));
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, kp);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;  // co-resident clusters of this configuration
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    max_clusters = n > 0 ? n : 1;
+  }
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, kp);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -538,16 +633,16 @@ cudaError_t launch_gemm(const GemmArgs& a, int sm_count, cudaStream_t stream, bo
   // 128-wide n-tiles when 256-wide ones would leave most SMs idle.
   const int64_t mt = (a.M + kBlockM - 1) / kBlockM;
   const bool narrow = a.N <= 128 || (!a.grouped && mt * ((a.N + 255) / 256) < sm_count);
-  if (a.grouped) {
+  if (a.grouped) {  // two m-tiles of a pair may belong to different experts: no pairs
     if (a.sb_row) return cudaErrorInvalidValue;
-    return narrow ? run<128, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed)
-                  : run<256, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
+    return narrow ? run<128, false, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                  : run<256, false, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
   }
   if (a.sb_row)
-    return narrow ? run<128, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
-                  : run<256, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
-  return narrow ? run<128, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
-                : run<256, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
+    return narrow ? run<128, true, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                  : run<256, true, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
+  return narrow ? run<128, false, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
+                : run<256, false, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
 }
 
 cudaError_t gemm_take_status(int* status) {
