@@ -28,6 +28,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 struct Divisor {
   float s;
   float r_lo, r_hi;
+  uint64_t r_lo2, r_hi2;  // {r_lo, r_lo} and {r_hi, r_hi} for packed FP32x2 multiplies
   bool fast;  // s is a normal float32; s == 0 and subnormal s take the exact path
 };
 
@@ -40,6 +41,51 @@ __device__ __forceinline__ Divisor make_divisor(float absmax) {
   // r_hi >= 1/s: r_lo itself when 1/s is exact (r_lo * s == 1, tested
   // exactly by one fused multiply-add), else the next float up.
   d.r_hi = (fmaf(d.r_lo, s, -1.0f) == 0.0f) ? d.r_lo : __uint_as_float(__float_as_uint(d.r_lo) + 1u);
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_lo2) : "f"(d.r_lo));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_hi2) : "f"(d.r_hi));
+  return d;
+}
+
+// Table-driven divisor.  For a normal BF16 absmax a = (1 + f/128) * 2^e the
+// scale is s = fl32(a / 448) = fl32((1 + f/128) / 448) * 2^e exactly, and
+// the reciprocal brackets scale by 2^-e in the same way (scaling by a power
+// of two commutes with rounding while everything stays normal).  So the
+// 128 values fl32((1 + f/128) / 448), their RD reciprocals and the RU
+// reciprocals are computed once per block with the IEEE intrinsics and the
+// per-group work is an exponent add.  Zero, subnormal or huge absmax values
+// take make_divisor.
+struct DivTable {
+  uint32_t s[128];     // bits of fl32((1 + f/128) / 448)
+  uint32_t rlo[128];   // bits of RD(1 / s)
+  uint32_t rhi[128];   // bits of RU(1 / s)
+};
+
+__device__ __forceinline__ void div_table_init(DivTable& t) {
+  for (int f = threadIdx.x; f < 128; f += blockDim.x) {
+    const float sf = __fdiv_rn(1.0f + static_cast<float>(f) * (1.0f / 128.0f), kE4M3Max);
+    const float lo = __frcp_rd(sf);
+    const float hi = (fmaf(lo, sf, -1.0f) == 0.0f) ? lo : __uint_as_float(__float_as_uint(lo) + 1u);
+    t.s[f] = __float_as_uint(sf);
+    t.rlo[f] = __float_as_uint(lo);
+    t.rhi[f] = __float_as_uint(hi);
+  }
+}
+
+// absmax given as BF16 bits (non-negative).
+__device__ __forceinline__ Divisor table_divisor(const DivTable& t, uint32_t a16) {
+  const uint32_t e = a16 >> 7;  // biased exponent of the absmax
+  // the scale (about 2^(e-127) / 448) and the reciprocals stay normal for
+  // biased exponents 10..254 of the absmax
+  if (e < 10 || e > 254) return make_divisor(__uint_as_float(a16 << 16));
+  const uint32_t f = a16 & 0x7Fu;
+  const int sh = static_cast<int>(e) - 127;
+  Divisor d;
+  d.s = __uint_as_float(t.s[f] + (static_cast<uint32_t>(sh) << 23));
+  d.r_lo = __uint_as_float(t.rlo[f] - (static_cast<uint32_t>(sh) << 23));
+  d.r_hi = __uint_as_float(t.rhi[f] - (static_cast<uint32_t>(sh) << 23));
+  d.fast = true;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_lo2) : "f"(d.r_lo));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_hi2) : "f"(d.r_hi));
   return d;
 }
 
@@ -54,26 +100,99 @@ __device__ __forceinline__ Divisor make_divisor(float absmax) {
 // divisions (quant8_exact).  The sign is applied last: the quotient has
 // x's sign, also for -0 and for results that round to zero.
 __device__ __forceinline__ uint32_t quant2(uint32_t w, const Divisor& d, bool& bad) {
-  const float a0 = fabsf(bf16_lo(w)), a1 = fabsf(bf16_hi(w));
-  const uint32_t c = e4m3x2(__fmul_rd(a0, d.r_lo), __fmul_rd(a1, d.r_lo));
-  const uint32_t c_hi = e4m3x2(__fmul_ru(a0, d.r_hi), __fmul_ru(a1, d.r_hi));
-  bad |= (c != c_hi);
-  return d.s == 0.0f ? 0u : (c | ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u));
+  // |x0|, |x1| as float32 bit patterns, multiplied pairwise (FP32x2) by the
+  // two reciprocal brackets with rounding down and up respectively.
+  const uint32_t aw = w & 0x7FFF7FFFu;
+  uint64_t av, lo, hi;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "r"(aw << 16), "r"(aw & 0xFFFF0000u));
+  asm("mul.rm.f32x2 %0, %1, %2;" : "=l"(lo) : "l"(av), "l"(d.r_lo2));
+  asm("mul.rp.f32x2 %0, %1, %2;" : "=l"(hi) : "l"(av), "l"(d.r_hi2));
+  float l0, l1, h0, h1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(l0), "=f"(l1) : "l"(lo));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(hi));
+  const uint32_t c = e4m3x2(l0, l1);
+  bad |= (c != e4m3x2(h0, h1));
+  return c | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
 }
 
-__device__ __forceinline__ float absmax8(uint4 v) {
-  const float m0 = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
-  const float m1 = fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)));
-  const float m2 = fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z)));
-  const float m3 = fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)));
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+// Largest |x| of BF16 values: for non-negative floats the integer order of
+// the bit patterns is the numeric order, so the magnitudes are compared as
+// unsigned 16-bit pairs (two per instruction).
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// Eight consecutive values -> eight codes (byte i = value i).
+__device__ __forceinline__ uint32_t absmax8_bits(uint4 v) {
+  const uint32_t k = 0x7FFF7FFFu;
+  return umax16x2(umax16x2(v.x & k, v.y & k), umax16x2(v.z & k, v.w & k));
+}
+
+// Packed |bf16| maximum -> float32.
+__device__ __forceinline__ float absmax_to_f32(uint32_t m) {
+  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+}
+
+__device__ __forceinline__ float absmax8(uint4 v) { return absmax_to_f32(absmax8_bits(v)); }
+
+// Eight consecutive values -> eight codes (byte i = value i).  The code
+// pairs of both brackets are packed and compared; the sign bits of the
+// inputs are gathered with one byte permute per word pair.  Bit j of
+// `badmask` is set when pair j (values 2j, 2j+1) needs the exact path.
+__device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& badmask) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t aw = w[j] & 0x7FFF7FFFu;
+    uint64_t av, l, h;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "r"(aw << 16), "r"(aw & 0xFFFF0000u));
+    asm("mul.rm.f32x2 %0, %1, %2;" : "=l"(l) : "l"(av), "l"(d.r_lo2));
+    asm("mul.rp.f32x2 %0, %1, %2;" : "=l"(h) : "l"(av), "l"(d.r_hi2));
+    float l0, l1, h0, h1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(l0), "=f"(l1) : "l"(l));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(h));
+    lo[j] = e4m3x2(l0, l1);
+    hi[j] = e4m3x2(h0, h1);
+    badmask |= (lo[j] != hi[j] || !d.fast) ? (1u << j) : 0u;
+  }
+  const uint32_t s0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
+  const uint32_t s1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
+  const uint32_t c0 = __byte_perm(lo[0], lo[1], 0x5410), c1 = __byte_perm(lo[2], lo[3], 0x5410);
+  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(c0 | s0, c1 | s1);
+}
+
 __device__ __forceinline__ uint2 quant8(uint4 v, const Divisor& d, bool& bad) {
-  bad |= !d.fast;
-  return make_uint2(quant2(v.x, d, bad) | (quant2(v.y, d, bad) << 16),
-                    quant2(v.z, d, bad) | (quant2(v.w, d, bad) << 16));
+  uint32_t m = 0;
+  const uint2 q = quant8m(v, d, m);
+  bad |= m != 0u;
+  return q;
+}
+
+// Codes of one value pair through IEEE divisions (x / s, then E4M3, sign
+// from the quotient): the exact path for a pair whose bracket straddles an
+// E4M3 rounding boundary.  Quotients of BF16 values close to such a
+// boundary are common (about 0.4% of the values of normal data), so the
+// fix-up is done per pair.
+__device__ __forceinline__ uint32_t quant2_exact(uint32_t w, float s) {
+  if (s == 0.0f) return 0u;
+  return e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
+}
+
+// Patches the pairs flagged in `badmask` of an 8-code chunk.
+__device__ __forceinline__ uint2 fix8(uint2 q, uint4 v, float s, uint32_t badmask) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[2] = {q.x, q.y};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (badmask & (1u << j)) {
+      const uint32_t e = quant2_exact(w[j], s);
+      const int sh = 16 * (j & 1);
+      c[j >> 1] = (c[j >> 1] & ~(0xFFFFu << sh)) | (e << sh);
+    }
+  }
+  return make_uint2(c[0], c[1]);
 }
 
 // The same codes through IEEE divisions, x / s then E4M3 (the fix-up path).
@@ -100,57 +219,74 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
-// 1x128 tiles.  Eight lanes own one group: lane l holds elements 8l..8l+7
-// and 64+8l..64+8l+7 (two 16-byte loads, each warp-wide load instruction
-// covering four contiguous 128-byte segments); a warp owns four consecutive
-// groups of the row-major (row, kb) enumeration, so consecutive warps stream
-// consecutive memory.  Each thread keeps 2*kUnroll 16-byte loads in flight.
-template <int kUnroll>
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M,
-                                                               int nkb, int64_t ldx, uint8_t* __restrict__ xq,
-                                                               float* __restrict__ sx) {
-  const int lane = threadIdx.x & 31;
-  const int sub = lane >> 3;
-  const int gl = lane & 7;
-  const int64_t K = static_cast<int64_t>(nkb) * kGroup;
-  const int64_t units = M * nkb;
-  const int64_t quads = (units + 3) >> 2;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+// 1x128 tiles.  A flat grid-stride stream over 16-value chunks: lane i of
+// the grid owns values 16i..16i+15 of the row-major group enumeration (two
+// 16-byte loads, one 16-byte store of codes), so eight consecutive lanes
+// form one 128-value group and a warp covers four contiguous groups.  The
+// (row, k-block) of a group comes from a multiply-high division by the
+// number of k-blocks.  Each lane loads its next chunk before quantising the
+// current one.
+__device__ __forceinline__ void group_rc(uint32_t g, uint64_t magic, int nkb, uint32_t& m, uint32_t& kb) {
+  // m = g / nkb with magic = ceil(2^40 / nkb): exact for g < 2^31, nkb < 512.
+  m = magic ? static_cast<uint32_t>((static_cast<uint64_t>(g) * magic) >> 40) : g / static_cast<uint32_t>(nkb);
+  kb = g - m * static_cast<uint32_t>(nkb);
+}
 
-  for (int64_t q0 = warp0; q0 < quads; q0 += nwarps * kUnroll) {
-    uint4 v0[kUnroll], v1[kUnroll];
-    int64_t m[kUnroll], kb[kUnroll];
-    bool ok[kUnroll];
-#pragma unroll
-    for (int i = 0; i < kUnroll; ++i) {
-      const int64_t u = 4 * (q0 + i * nwarps) + sub;
-      ok[i] = u < units;
-      m[i] = ok[i] ? u / nkb : 0;
-      kb[i] = ok[i] ? u - m[i] * nkb : 0;
-      const uint16_t* p = x + m[i] * ldx + kb[i] * kGroup + gl * 8;
-      v0[i] = ok[i] ? ld_stream_16(p) : make_uint4(0, 0, 0, 0);
-      v1[i] = ok[i] ? ld_stream_16(p + 64) : make_uint4(0, 0, 0, 0);
+struct Chunk16 {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ void chunk_load(Chunk16& c, const uint16_t* __restrict__ x, int64_t i, int64_t n16,
+                                           uint64_t magic, int nkb, int64_t ldx) {
+  if (i < n16) {
+    uint32_t m, kb;
+    group_rc(static_cast<uint32_t>(i >> 3), magic, nkb, m, kb);
+    const uint16_t* p = x + static_cast<int64_t>(m) * ldx + static_cast<int64_t>(kb) * kGroup + (i & 7) * 16;
+    c.a = ld_stream_16(p);
+    c.b = ld_stream_16(p + 8);
+  } else {
+    c.a = make_uint4(0, 0, 0, 0);
+    c.b = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M,
+                                                               int nkb, int64_t ldx, uint64_t magic,
+                                                               uint8_t* __restrict__ xq, float* __restrict__ sx) {
+  __shared__ DivTable tab;
+  div_table_init(tab);
+  __syncthreads();
+  const int64_t n16 = M * nkb * 8;  // 16-value chunks
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t K = static_cast<int64_t>(nkb) * kGroup;
+  // Warp-uniform trip count: every lane of a warp runs the same number of
+  // steps (out-of-range chunks are zeros and are not stored), so the group
+  // shuffles always see all 32 lanes.
+  const int64_t warp_first = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  Chunk16 cur;
+  chunk_load(cur, x, i, n16, magic, nkb, ldx);
+  for (int64_t w0 = warp_first; w0 < n16; w0 += nthreads, i += nthreads) {
+    Chunk16 nxt;
+    chunk_load(nxt, x, i + nthreads, n16, magic, nkb, ldx);
+    uint32_t am = umax16x2(absmax8_bits(cur.a), absmax8_bits(cur.b));
+    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    const Divisor d = table_divisor(tab, max(am & 0xFFFFu, am >> 16));
+    uint32_t bad_a = 0, bad_b = 0;
+    uint2 qa = quant8m(cur.a, d, bad_a);
+    uint2 qb = quant8m(cur.b, d, bad_b);
+    if (bad_a) qa = fix8(qa, cur.a, d.s, bad_a);
+    if (bad_b) qb = fix8(qb, cur.b, d.s, bad_b);
+    if (i < n16) {
+      uint32_t m, kb;
+      group_rc(static_cast<uint32_t>(i >> 3), magic, nkb, m, kb);
+      *reinterpret_cast<uint4*>(xq + static_cast<int64_t>(m) * K + static_cast<int64_t>(kb) * kGroup + (i & 7) * 16) =
+          make_uint4(qa.x, qa.y, qb.x, qb.y);
+      if ((i & 7) == 0) sx[static_cast<int64_t>(kb) * M + m] = d.s;
     }
-#pragma unroll
-    for (int i = 0; i < kUnroll; ++i) {
-      float a = fmaxf(absmax8(v0[i]), absmax8(v1[i]));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      const Divisor d = make_divisor(a);
-      bool bad0 = false, bad1 = false;
-      uint2 q0v = quant8(v0[i], d, bad0);
-      uint2 q1v = quant8(v1[i], d, bad1);
-      if (bad0) q0v = quant8_exact(v0[i], d.s);
-      if (bad1) q1v = quant8_exact(v1[i], d.s);
-      if (ok[i]) {
-        uint8_t* o = xq + m[i] * K + kb[i] * kGroup + gl * 8;
-        *reinterpret_cast<uint2*>(o) = q0v;
-        *reinterpret_cast<uint2*>(o + 64) = q1v;
-        if (gl == 0) sx[kb[i] * M + m[i]] = d.s;
-      }
-    }
+    cur = nxt;
   }
 }
 
@@ -166,7 +302,7 @@ __device__ __forceinline__ uint2 quant_col8(const uint4 (&v)[8], int i, const Di
   uint32_t p[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) p[j] = quant2(col16(v[2 * j], i) | (col16(v[2 * j + 1], i) << 16), d, bad);
-  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
 // Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
@@ -334,15 +470,23 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
 
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
                                       float* sx, int sm_count, cudaStream_t stream) {
-  constexpr int kUnroll = 2;
   const int nkb = static_cast<int>(K / kGroup);
-  const int64_t quads = (M * nkb + 3) / 4;
-  const int64_t warps_needed = (quads + kUnroll - 1) / kUnroll;
-  const int64_t blocks_needed = (warps_needed + 7) / 8;
-  const int64_t max_blocks = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM
+  const int64_t n16 = M * nkb * 8;
+  if (n16 >= (int64_t(1) << 34)) return cudaErrorInvalidValue;  // group index must fit 31 bits
+  // ceil(2^40 / nkb): the multiply-high division is exact for nkb < 512
+  const uint64_t magic = nkb < 512 ? ((uint64_t(1) << 40) + nkb - 1) / nkb : 0;
+  static int per_sm = 0;  // resident 256-thread blocks per SM
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_act_1x128_kernel, 256, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const int64_t blocks_needed = (n16 + 255) / 256;
+  const int64_t max_blocks = static_cast<int64_t>(sm_count) * per_sm;
   const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
   if (blocks <= 0) return cudaSuccess;
-  quant_act_1x128_kernel<kUnroll><<<blocks, 256, 0, stream>>>(x, M, nkb, ldx, xq, sx);
+  quant_act_1x128_kernel<<<blocks, 256, 0, stream>>>(x, M, nkb, ldx, magic, xq, sx);
   return cudaGetLastError();
 }
 
