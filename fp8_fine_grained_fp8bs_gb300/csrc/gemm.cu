@@ -94,36 +94,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// acc[j] += p[j] * s for 32 accumulators, two per packed FP32x2 FMA.
-__device__ __forceinline__ void fold_block(float* acc, const uint32_t (&p)[32], float s) {
+// acc[j] += p[j] * s for 32 accumulators (16 pairs), one packed FP32x2
+// FMA per pair.
+__device__ __forceinline__ void fold_block(float2* acc, const uint32_t (&p)[32], float s) {
+  const float2 s2 = make_float2(s, s);
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    asm("{\n\t.reg .b64 a, q, c;\n\t"
-        "mov.b64 a, {%0, %1};\n\t"
-        "mov.b64 q, {%2, %3};\n\t"
-        "mov.b64 c, {%4, %4};\n\t"
-        "fma.rn.f32x2 a, q, c, a;\n\t"
-        "mov.b64 {%0, %1}, a;\n}"
-        : "+f"(acc[j]), "+f"(acc[j + 1])
-        : "r"(p[j]), "r"(p[j + 1]), "f"(s));
-  }
+  for (int j = 0; j < 16; ++j)
+    acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), s2, acc[j]);
 }
 
 // acc[j] += p[j] * (s_a * s_b[j]) with per-column scales s_b (Wgrad).
-__device__ __forceinline__ void fold_row(float* acc, const uint32_t (&p)[32], float sa, const float* sb) {
+__device__ __forceinline__ void fold_row(float2* acc, const uint32_t (&p)[32], float sa, const float* sb) {
+  const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    const float2 b = *reinterpret_cast<const float2*>(sb + j);
-    asm("{\n\t.reg .b64 a, q, c, t;\n\t"
-        "mov.b64 t, {%4, %4};\n\t"
-        "mov.b64 c, {%5, %6};\n\t"
-        "mul.rn.f32x2 c, c, t;\n\t"
-        "mov.b64 a, {%0, %1};\n\t"
-        "mov.b64 q, {%2, %3};\n\t"
-        "fma.rn.f32x2 a, q, c, a;\n\t"
-        "mov.b64 {%0, %1}, a;\n}"
-        : "+f"(acc[j]), "+f"(acc[j + 1])
-        : "r"(p[j]), "r"(p[j + 1]), "f"(sa), "f"(b.x), "f"(b.y));
+  for (int j = 0; j < 16; ++j) {
+    const float2 c = __fmul2_rn(sa2, *reinterpret_cast<const float2*>(sb + 2 * j));
+    acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), c, acc[j]);
   }
 }
 
@@ -413,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool mvalid = m < p.M;
       const int ncol0 = n0 + colhalf * C::kColsPerThread;
       const int bsel = (colhalf * C::kColsPerThread) / 128;   // which 128-column block of the tile
-      float acc[C::kColsPerThread];
+      float2 acc2[C::kColsPerThread / 2];
 #pragma unroll
-      for (int j = 0; j < C::kColsPerThread; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < C::kColsPerThread / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
       for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
         if (!mbar_wait(&sc_full[slot], sph, p.timeout_ns)) { live = false; break; }
         if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
@@ -446,11 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (kRowScale) {
-            fold_row(acc + ch * 32, ra, s_ab, scol + ch * 32);
-            fold_row(acc + (ch + 1) * 32, rb, s_ab, scol + (ch + 1) * 32);
+            fold_row(acc2 + ch * 16, ra, s_ab, scol + ch * 32);
+            fold_row(acc2 + (ch + 1) * 16, rb, s_ab, scol + (ch + 1) * 32);
           } else {
-            fold_block(acc + ch * 32, ra, s_ab);
-            fold_block(acc + (ch + 1) * 32, rb, s_ab);
+            fold_block(acc2 + ch * 16, ra, s_ab);
+            fold_block(acc2 + (ch + 1) * 16, rb, s_ab);
           }
         }
         __syncwarp();
@@ -461,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!live) break;
       // ---- store this thread's row segment
+      const float* acc = reinterpret_cast<const float*>(acc2);
       if (mvalid && ncol0 < p.N) {
         if (p.out_bf16) {
           __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) + m * p.N + ncol0;

@@ -100,18 +100,12 @@ __device__ __forceinline__ Divisor table_divisor(const DivTable& t, uint32_t a16
 // divisions (quant8_exact).  The sign is applied last: the quotient has
 // x's sign, also for -0 and for results that round to zero.
 __device__ __forceinline__ uint32_t quant2(uint32_t w, const Divisor& d, bool& bad) {
-  // |x0|, |x1| as float32 bit patterns, multiplied pairwise (FP32x2) by the
-  // two reciprocal brackets with rounding down and up respectively.
   const uint32_t aw = w & 0x7FFF7FFFu;
-  uint64_t av, lo, hi;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "r"(aw << 16), "r"(aw & 0xFFFF0000u));
-  asm("mul.rm.f32x2 %0, %1, %2;" : "=l"(lo) : "l"(av), "l"(d.r_lo2));
-  asm("mul.rp.f32x2 %0, %1, %2;" : "=l"(hi) : "l"(av), "l"(d.r_hi2));
-  float l0, l1, h0, h1;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(l0), "=f"(l1) : "l"(lo));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(hi));
-  const uint32_t c = e4m3x2(l0, l1);
-  bad |= (c != e4m3x2(h0, h1));
+  const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
+  const float2 l = __fmul2_rd(a, make_float2(d.r_lo, d.r_lo));
+  const float2 h = __fmul2_ru(a, make_float2(d.r_hi, d.r_hi));
+  const uint32_t c = e4m3x2(l.x, l.y);
+  bad |= (c != e4m3x2(h.x, h.y));
   return c | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
 }
 
@@ -142,19 +136,18 @@ __device__ __forceinline__ float absmax8(uint4 v) { return absmax_to_f32(absmax8
 // `badmask` is set when pair j (values 2j, 2j+1) needs the exact path.
 __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& badmask) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float2 rlo = make_float2(d.r_lo, d.r_lo), rhi = make_float2(d.r_hi, d.r_hi);
   uint32_t lo[4], hi[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    // |x| of both halves as float32, times the brackets with rounding down
+    // and up (packed FP32x2 multiplies)
     const uint32_t aw = w[j] & 0x7FFF7FFFu;
-    uint64_t av, l, h;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "r"(aw << 16), "r"(aw & 0xFFFF0000u));
-    asm("mul.rm.f32x2 %0, %1, %2;" : "=l"(l) : "l"(av), "l"(d.r_lo2));
-    asm("mul.rp.f32x2 %0, %1, %2;" : "=l"(h) : "l"(av), "l"(d.r_hi2));
-    float l0, l1, h0, h1;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(l0), "=f"(l1) : "l"(l));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(h));
-    lo[j] = e4m3x2(l0, l1);
-    hi[j] = e4m3x2(h0, h1);
+    const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
+    const float2 l = __fmul2_rd(a, rlo);
+    const float2 h = __fmul2_ru(a, rhi);
+    lo[j] = e4m3x2(l.x, l.y);
+    hi[j] = e4m3x2(h.x, h.y);
     badmask |= (lo[j] != hi[j] || !d.fast) ? (1u << j) : 0u;
   }
   const uint32_t s0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
