@@ -65,8 +65,10 @@ int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t
   if (st != FP8BS_OK) return st;
   const auto* xb = static_cast<const uint16_t*>(x);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (xq_t != nullptr) return from_cuda(fp8bs::launch_quantize_act_dual(xb, M, K, ldx, xq, sx, xq_t, sx_t, s));
-  return from_cuda(fp8bs::launch_quantize_act_1x128(xb, M, K, ldx, xq, sx, sms, s));
+  const uint64_t tmo = g_timeout_ns.load();
+  if (xq_t != nullptr)
+    return from_cuda(fp8bs::launch_quantize_act_dual(xb, M, K, ldx, xq, sx, xq_t, sx_t, sms, tmo, s));
+  return from_cuda(fp8bs::launch_quantize_act_1x128(xb, M, K, ldx, xq, sx, sms, tmo, s));
 }
 
 int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw, uint8_t* wq_t,
@@ -81,8 +83,8 @@ int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint
   int sms = 0;
   const int st = current_device(&sms);
   if (st != FP8BS_OK) return st;
-  return from_cuda(fp8bs::launch_quantize_weight(static_cast<const uint16_t*>(w), N, K, ldw, wq, sw, wq_t, sw_t,
-                                                 static_cast<cudaStream_t>(stream)));
+  return from_cuda(fp8bs::launch_quantize_weight(static_cast<const uint16_t*>(w), N, K, ldw, wq, sw, wq_t, sw_t, sms,
+                                                 g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
 }
 
 static int run_gemm(const fp8bs::GemmArgs& args, void* stream) {
@@ -144,9 +146,10 @@ int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const
 
 int fp8bs_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-  int v = 0;
+  int v = 0, q = 0;
   if (fp8bs::gemm_take_status(&v) != cudaSuccess) return FP8BS_ERR_CUDA;
-  return v;
+  if (fp8bs::quant_take_status(&q) != cudaSuccess) return FP8BS_ERR_CUDA;
+  return v != FP8BS_OK ? v : q;
 }
 
 int fp8bs_set_wait_timeout_ms(int64_t ms) {

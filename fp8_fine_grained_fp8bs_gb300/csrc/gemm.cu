@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fp8bs {
 namespace {
@@ -47,8 +48,16 @@ constexpr int kBlockM = 128;
 constexpr int kBlockK = 128;         // = N_C
 constexpr int kUmmaK = 32;           // K of one kind::f8f6f4 MMA (bytes of E4M3)
 constexpr int kMaxGroups = 512;
-constexpr int kScaleSlots = 16;      // scale ring depth (k-blocks the loader may run ahead)
-constexpr uint32_t kTmemCols = 512;  // two partial buffers of up to 256 columns
+// Scale ring: kScaleSlots k-blocks of scales, handed between the loader
+// and the epilogue in chunks of kScaleChunk slots.  Every mbarrier
+// operation costs the epilogue warps a shared-memory round trip of some
+// 170 cycles while TMA and the tensor core keep shared memory busy, and
+// each epilogue warp handles every k-block, so the hand-off is per chunk
+// rather than per k-block.
+constexpr int kScaleChunk = 8;
+constexpr int kScaleChunks = 2;
+constexpr int kScaleSlots = kScaleChunk * kScaleChunks;
+constexpr uint32_t kTmemCols = 512;  // all of TMEM: 512 / BN partial buffers
 constexpr uint32_t kRegsProducer = 56;
 constexpr uint32_t kRegsEpilogue = 224;
 
@@ -58,7 +67,12 @@ template <int BN, bool kPair>
 struct Cfg {
   static constexpr int kABytes = kBlockM * kBlockK;                   // 16 KB
   static constexpr int kBBytes = (kPair ? BN / 2 : BN) * kBlockK;     // 16 or 32 KB per CTA
-  static constexpr int kStages = (kABytes + kBBytes) == 48 * 1024 ? 4 : 6;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kStageBytes >= 48 * 1024 ? 4 : kStageBytes >= 32 * 1024 ? 6 : 8;
+  // TMEM partial buffers: the MMA of k-block j+kBufs may start only once
+  // the epilogue has read k-block j out, so more buffers hide more of that
+  // hand-off (commit, TMEM read-out, release) behind tensor-core work.
+  static constexpr int kBufs = static_cast<int>(kTmemCols) / BN;
   static constexpr int kSlotFloats = kBlockM + BN;        // A row scales, then B column scales
   static constexpr int kColsPerThread = BN / 2;
   static constexpr int kChunks = kColsPerThread / 32;
@@ -67,7 +81,7 @@ struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffScale = kOffB + kStages * kBBytes;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
-  static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 4 + 2;
+  static constexpr int kNumBars = 2 * kStages + 2 * kScaleChunks + 2 * kBufs + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;       // tmem slot, abort flag, tile count
   static constexpr int kOffGroups = kOffMisc + 16;              // offsets[G+1], cum[G+1]
   static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
@@ -160,11 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full = bars;                               // [kStages] TMA -> MMA
   uint64_t* empty = bars + C::kStages;                 // [kStages] MMA -> TMA
-  uint64_t* sc_full = bars + 2 * C::kStages;           // [kScaleSlots] scales landed
-  uint64_t* sc_empty = sc_full + kScaleSlots;          // [kScaleSlots] epilogue done with them
-  uint64_t* t_full = sc_empty + kScaleSlots;           // [2] partial ready in TMEM
-  uint64_t* t_empty = t_full + 2;                      // [2] partial read out of TMEM
-  uint64_t* teardown = t_full + 4;                     // [2] one per MMA issuer
+  uint64_t* sc_full = bars + 2 * C::kStages;           // [kScaleChunks] scales landed
+  uint64_t* sc_empty = sc_full + kScaleChunks;         // [kScaleChunks] epilogue done with them
+  uint64_t* t_full = sc_empty + kScaleChunks;          // [kBufs] partial ready in TMEM
+  uint64_t* t_empty = t_full + C::kBufs;               // [kBufs] partial read out of TMEM
+  uint64_t* teardown = t_empty + C::kBufs;             // [2] one per MMA issuer
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* s_off = reinterpret_cast<int*>(smem + C::kOffGroups);
   int* s_cum = s_off + (kMaxGroups + 1);
@@ -183,11 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kScaleSlots; ++s) {
+    for (int s = 0; s < kScaleChunks; ++s) {
       mbar_init(&sc_full[s], 32);                      // one cp.async arrival per loader lane
       mbar_init(&sc_empty[s], kEpiThreads / 32);       // one arrival per epilogue warp
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kBufs; ++b) {
       mbar_init(&t_full[b], 1);
       mbar_init(&t_empty[b], (kPair ? 2 : 1) * kEpiThreads / 32);  // with pairs: both CTAs' epilogue warps
     }
@@ -292,15 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if ((warp == 1 || warp == 3) && lane == 0 && rank == 0) {
       // --------------------------------------------------------- MMA issuers
-      // Two issuing threads on different SM sub-partitions take alternate
-      // k-block steps (warp 1 the even ones, warp 3 the odd ones), so each
-      // owns one TMEM buffer.  Issuing MMAs holds up tcgen05.ld on the
-      // issuer's sub-partition; splitting the issue halves that stall for
-      // the epilogue warps that share it.  With pairs only the leader CTA
-      // issues: one M=256 MMA covers both CTAs.
+      // Two issuing threads take alternate k-block steps (warp 1 the even
+      // ones, warp 3 the odd ones): issuing a k-block's MMAs blocks the
+      // issuing thread for about as long as the tensor core takes to
+      // accept them, so one thread can prepare the next step while the
+      // other's MMAs drain.  Step s uses TMEM buffer s % kBufs.  With pairs
+      // only the leader CTA issues: one M=256 MMA covers both CTAs.
       constexpr uint32_t idesc = idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, BN);
       const uint32_t parity = warp == 1 ? 0u : 1u;
-      const uint32_t buf = parity;
       uint32_t step = 0;
       bool live = true;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
@@ -308,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((step & 1u) != parity) continue;
           const int stage = static_cast<int>(step % C::kStages);
           const uint32_t phase = (step / C::kStages) & 1u;
-          const uint32_t tphase = (step >> 1) & 1u;
+          const uint32_t buf = step % C::kBufs;
+          const uint32_t tphase = (step / C::kBufs) & 1u;
           if (!mbar_wait(&full[stage], phase, p.timeout_ns)) { live = false; break; }
           if (!mbar_wait(&t_empty[buf], tphase ^ 1, p.timeout_ns)) { live = false; break; }
           tc_fence_after_sync();
@@ -344,16 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ----------------------------------------------------- scale loader
       // Slot layout: [0,128) row scales of A for the tile's 128 rows,
       // [128, 128+BN) B scales: per column (row kind) or, for 128x128
-      // block scales, one per 128-column block of the tile.
-      int slot = 0;
-      uint32_t sph = 0;
+      // block scales, one per 128-column block of the tile.  Step s (the
+      // CTA's s-th k-block over all its tiles) uses slot s % kScaleSlots;
+      // a chunk is announced once its last slot is issued (or at the CTA's
+      // final step).
+      uint32_t step = 0;
       bool live = true;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
         int row0, n0, g;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
-        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
-          if (!mbar_wait(&sc_empty[slot], sph ^ 1, p.timeout_ns)) { live = false; break; }
-          float* dst = sScale + slot * C::kSlotFloats;
+        const bool last_tile = t + nunits >= total_tiles;
+        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, ++step, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
+          const uint32_t chunk = (step / kScaleChunk) % kScaleChunks;
+          if (step % kScaleChunk == 0 &&
+              !mbar_wait(&sc_empty[chunk], ((step / kScaleSlots) & 1u) ^ 1u, p.timeout_ns)) {
+            live = false;
+            break;
+          }
+          float* dst = sScale + (step % kScaleSlots) * C::kSlotFloats;
           const float* sa_kb = p.sa + static_cast<int64_t>(kb) * p.M;
 #pragma unroll
           for (int i = 0; i < kBlockM / 32; ++i) {
@@ -371,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nb = static_cast<int64_t>(g) * nnb + n0 / 128 + lane;
             cp_async_4(dst + kBlockM + lane, p.sb + nb * p.nkb + kb);
           }
-          cp_async_mbar_arrive(&sc_full[slot]);
-          if (++slot == kScaleSlots) { slot = 0; sph ^= 1; }
+          if (step % kScaleChunk == kScaleChunk - 1 || (last_tile && kk + 1 == p.nkb))
+            cp_async_mbar_arrive(&sc_full[chunk]);
         }
       }
       if (!live) {
@@ -389,8 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int colhalf = e >> 2;          // which BN/2 columns
     const int row_in_tile = quarter * 32 + lane;
     uint32_t buf = 0, tphase = 0;
-    int slot = 0;
-    uint32_t sph = 0;
+    uint32_t step = 0;
     bool live = true;
     for (int t = unit0; t < total_tiles && live; t += nunits) {
       int row0, n0, g;
@@ -402,11 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 acc2[C::kColsPerThread / 2];
 #pragma unroll
       for (int j = 0; j < C::kColsPerThread / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
-      for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
-        if (!mbar_wait(&sc_full[slot], sph, p.timeout_ns)) { live = false; break; }
+      for (int kk = 0; kk < p.nkb; ++kk, ++step) {
+        const uint32_t chunk = (step / kScaleChunk) % kScaleChunks;
+        if (step % kScaleChunk == 0 &&
+            !mbar_wait(&sc_full[chunk], (step / kScaleSlots) & 1u, p.timeout_ns)) {
+          live = false;
+          break;
+        }
         if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
         tc_fence_after_sync();
-        const float* scs = sScale + slot * C::kSlotFloats;
+        const float* scs = sScale + (step % kScaleSlots) * C::kSlotFloats;
         const float sa = scs[row_in_tile];
         const float s_ab = kRowScale ? sa : sa * scs[kBlockM + bsel];
         const float* scol = scs + kBlockM + colhalf * C::kColsPerThread;
@@ -439,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fold_block(acc2 + (ch + 1) * 16, rb, s_ab);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sc_empty[slot]);
-        if (++slot == kScaleSlots) { slot = 0; sph ^= 1; }
-        buf ^= 1;
-        if (buf == 0) tphase ^= 1;
+        if (step % kScaleChunk == kScaleChunk - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sc_empty[chunk]);
+        }
+        if (++buf == C::kBufs) { buf = 0; tphase ^= 1; }
       }
       if (!live) break;
       // ---- store this thread's row segment
@@ -493,26 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // K-major E4M3 operand [outer...][inner=K] with a 128 x box_rows box and
 // 128-byte swizzling (one 128-byte row of K per box row).
 bool encode_operand(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                     uint32_t box_rows) {
-  auto enc = get_encode();
+  auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t gdim[3];
   cuuint64_t gstride[2];

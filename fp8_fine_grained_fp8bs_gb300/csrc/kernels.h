@@ -8,12 +8,20 @@
 namespace fp8bs {
 
 // ---- quantize.cu
+// Every quantiser streams 128x128 BF16 tiles through shared memory with
+// TMA; its waits are bounded by timeout_ns and a wait that expires records
+// FP8BS_ERR_TIMEOUT in the status word that quant_take_status reads.
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                      float* sx, int sm_count, cudaStream_t stream);
+                                      float* sx, int sm_count, uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                     float* sx, uint8_t* xq_t, float* sx_t, cudaStream_t stream);
+                                     float* sx, uint8_t* xq_t, float* sx_t, int sm_count, uint64_t timeout_ns,
+                                     cudaStream_t stream);
 cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
-                                   float* sw, uint8_t* wq_t, float* sw_t, cudaStream_t stream);
+                                   float* sw, uint8_t* wq_t, float* sw_t, int sm_count, uint64_t timeout_ns,
+                                   cudaStream_t stream);
+// Reads and clears the quantisers' device status word (synchronous copy on
+// the current device).
+cudaError_t quant_take_status(int* status);
 
 // ---- gemm.cu
 struct GemmArgs {
@@ -39,9 +47,8 @@ struct GemmArgs {
 cudaError_t launch_gemm(const GemmArgs& args, int sm_count, cudaStream_t stream, bool* tmap_failed,
                         bool* reg_check_failed);
 
-// Reads and clears the device status word of the GEMM kernels (the only
-// kernels with waits or device-side argument checks); synchronous copy on
-// the current device.
+// Reads and clears the device status word of the GEMM kernels; synchronous
+// copy on the current device.
 cudaError_t gemm_take_status(int* status);
 
 }  // namespace fp8bs

@@ -12,12 +12,10 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fp8bs {
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Two float32 -> two E4M3 codes (RNE, saturating to +-448); a in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
@@ -156,13 +154,6 @@ __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& ba
   return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(c0 | s0, c1 | s1);
 }
 
-__device__ __forceinline__ uint2 quant8(uint4 v, const Divisor& d, bool& bad) {
-  uint32_t m = 0;
-  const uint2 q = quant8m(v, d, m);
-  bad |= m != 0u;
-  return q;
-}
-
 // Codes of one value pair through IEEE divisions (x / s, then E4M3, sign
 // from the quotient): the exact path for a pair whose bracket straddles an
 // E4M3 rounding boundary.  Quotients of BF16 values close to such a
@@ -193,94 +184,6 @@ __device__ __forceinline__ uint32_t quant1_exact(uint32_t h, float s) {
   if (s == 0.0f) return 0u;
   const float q = __fdiv_rn(__uint_as_float(h << 16), s);
   return e4m3x2(q, 0.0f) & 0xFFu;
-}
-
-__device__ __forceinline__ uint2 quant8_exact(uint4 v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t b[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) b[i] = quant1_exact((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu), s);
-  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
-}
-
-__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// ---------------------------------------------------------------------------
-// 1x128 tiles.  A flat grid-stride stream over 16-value chunks: lane i of
-// the grid owns values 16i..16i+15 of the row-major group enumeration (two
-// 16-byte loads, one 16-byte store of codes), so eight consecutive lanes
-// form one 128-value group and a warp covers four contiguous groups.  The
-// (row, k-block) of a group comes from a multiply-high division by the
-// number of k-blocks.  Each lane loads its next chunk before quantising the
-// current one.
-__device__ __forceinline__ void group_rc(uint32_t g, uint64_t magic, int nkb, uint32_t& m, uint32_t& kb) {
-  // m = g / nkb with magic = ceil(2^40 / nkb): exact for g < 2^31, nkb < 512.
-  m = magic ? static_cast<uint32_t>((static_cast<uint64_t>(g) * magic) >> 40) : g / static_cast<uint32_t>(nkb);
-  kb = g - m * static_cast<uint32_t>(nkb);
-}
-
-struct Chunk16 {
-  uint4 a, b;
-};
-
-__device__ __forceinline__ void chunk_load(Chunk16& c, const uint16_t* __restrict__ x, int64_t i, int64_t n16,
-                                           uint64_t magic, int nkb, int64_t ldx) {
-  if (i < n16) {
-    uint32_t m, kb;
-    group_rc(static_cast<uint32_t>(i >> 3), magic, nkb, m, kb);
-    const uint16_t* p = x + static_cast<int64_t>(m) * ldx + static_cast<int64_t>(kb) * kGroup + (i & 7) * 16;
-    c.a = ld_stream_16(p);
-    c.b = ld_stream_16(p + 8);
-  } else {
-    c.a = make_uint4(0, 0, 0, 0);
-    c.b = make_uint4(0, 0, 0, 0);
-  }
-}
-
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M,
-                                                               int nkb, int64_t ldx, uint64_t magic,
-                                                               uint8_t* __restrict__ xq, float* __restrict__ sx) {
-  __shared__ DivTable tab;
-  div_table_init(tab);
-  __syncthreads();
-  const int64_t n16 = M * nkb * 8;  // 16-value chunks
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t K = static_cast<int64_t>(nkb) * kGroup;
-  // Warp-uniform trip count: every lane of a warp runs the same number of
-  // steps (out-of-range chunks are zeros and are not stored), so the group
-  // shuffles always see all 32 lanes.
-  const int64_t warp_first = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  Chunk16 cur;
-  chunk_load(cur, x, i, n16, magic, nkb, ldx);
-  for (int64_t w0 = warp_first; w0 < n16; w0 += nthreads, i += nthreads) {
-    Chunk16 nxt;
-    chunk_load(nxt, x, i + nthreads, n16, magic, nkb, ldx);
-    uint32_t am = umax16x2(absmax8_bits(cur.a), absmax8_bits(cur.b));
-    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 2));
-    am = umax16x2(am, __shfl_xor_sync(0xffffffffu, am, 4));
-    const Divisor d = table_divisor(tab, max(am & 0xFFFFu, am >> 16));
-    uint32_t bad_a = 0, bad_b = 0;
-    uint2 qa = quant8m(cur.a, d, bad_a);
-    uint2 qb = quant8m(cur.b, d, bad_b);
-    if (bad_a) qa = fix8(qa, cur.a, d.s, bad_a);
-    if (bad_b) qb = fix8(qb, cur.b, d.s, bad_b);
-    if (i < n16) {
-      uint32_t m, kb;
-      group_rc(static_cast<uint32_t>(i >> 3), magic, nkb, m, kb);
-      *reinterpret_cast<uint4*>(xq + static_cast<int64_t>(m) * K + static_cast<int64_t>(kb) * kGroup + (i & 7) * 16) =
-          make_uint4(qa.x, qa.y, qb.x, qb.y);
-      if ((i & 7) == 0) sx[static_cast<int64_t>(kb) * M + m] = d.s;
-    }
-    cur = nxt;
-  }
 }
 
 // BF16 bits of column i (0..7) of an 8-value row chunk.
@@ -314,192 +217,461 @@ __device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
   return make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
 }
 
-// Exact fix-up of one 8-row column chunk, re-reading the BF16 inputs.
-__device__ __noinline__ uint2 quant_col8_exact(const uint16_t* x, int64_t ld, float s) {
+// Exact codes of column i of rows 0..7 through IEEE divisions (the fix-up
+// path of quant_col8).
+__device__ __noinline__ uint2 quant_col8_exact(const uint4 (&v)[8], int i, float s) {
   uint32_t b[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = quant1_exact(x[j * ld], s);
+  for (int j = 0; j < 8; ++j) b[j] = quant1_exact(col16(v[j], i), s);
   return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
-// Exact fix-up of one 8-value row chunk, re-reading the BF16 inputs.
-__device__ __noinline__ uint2 quant_row8_exact(const uint16_t* x, float s) {
-  return quant8_exact(*reinterpret_cast<const uint4*>(x), s);
+// ---------------------------------------------------------------------------
+// Tile pipeline.  The BF16 input is cut into 128x128 tiles (128 rows of one
+// 128-column block).  A producer warp streams the tiles with TMA into a ring
+// of shared-memory stages; eight compute warps quantise each tile out of
+// shared memory and store codes and scales with coalesced writes.  Loads are
+// thereby decoupled from the arithmetic: several tiles per SM are in flight
+// while the warps compute, which a load-then-compute kernel cannot sustain.
+//
+// Two thread layouts:
+//  - row layout (1x128 groups, and weights without the transposed copy):
+//    thread t owns the 64 values of half t%2 of tile row t/2, so a row's
+//    absmax is one shuffle away and each thread derives one divisor per
+//    tile.  TMA stores the two 64-column halves of the tile as separate
+//    boxes with 128-byte swizzling (chunk i of a 128-byte row r lands at
+//    chunk i ^ (r % 8)), and the thread's i-th load reads logical chunk
+//    (i + 4 * half) % 8: the eight lanes of a quarter-warp then read eight
+//    different bank groups.
+//  - block layout (128x1 groups, transposed codes): thread t owns rows
+//    8*(t/16) .. +7 of the 8-column chunk t%16 (an 8x8 sub-block whose
+//    transpose is a byte permutation in registers); the tile is stored
+//    unswizzled and a quarter-warp reads 128 consecutive bytes of a row.
+enum TileMode : int {
+  kModeAct = 0,      // 1x128 groups, row layout
+  kModeWeight = 1,   // one 128x128 group per tile, row layout
+  kModeWeightT = 2,  // one 128x128 group per tile plus the transposed codes, block layout
+  kModeDual = 3      // 1x128 and 128x1 groups, block layout
+};
+
+template <int kMode>
+struct QCfg {
+  static constexpr bool kRowLayout = kMode == kModeAct || kMode == kModeWeight;
+  static constexpr int kStages = kRowLayout ? 3 : 4;
+  static constexpr int kMinBlocks = kRowLayout ? 2 : 1;  // CTAs per SM the registers are budgeted for
+};
+
+constexpr int kQComputeThreads = 256;
+constexpr int kQThreads = kQComputeThreads + 32;  // + the producer warp
+constexpr int kTileBytes = kGroup * kGroup * 2;    // 32 KB of BF16
+constexpr int kTileRowBytes = kGroup * 2;
+constexpr int kQMaxStages = 4;
+
+struct TileParams {
+  int64_t rows;     // rows of the input (M, or N for a weight)
+  int64_t nrb;      // row blocks, ceil(rows / 128)
+  int nkb;          // column blocks, K / 128
+  uint8_t* q;       // [rows][K] codes (1x128 groups, or the weight's blocks)
+  float* s;         // act, dual: [nkb][rows]; weight: [nrb][nkb]
+  uint8_t* q_t;     // dual: [K][rows] codes of the 128x1 groups; weight: transposed codes; or null
+  float* s_t;       // dual: [nrb][K]; weight: [nkb][nrb]; or null
+  uint64_t timeout_ns;
+};
+
+struct QShared {
+  uint64_t full[kQMaxStages];
+  uint64_t empty[kQMaxStages];
+  DivTable tab;
+  uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
+  uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
+  uint32_t colmax[kGroup / 2];                         // dual: column maxima of the tile, two per word
+};
+
+template <int kMode>
+constexpr int q_smem_bytes() {
+  return QCfg<kMode>::kStages * kTileBytes + static_cast<int>(sizeof(QShared)) + 1024;
 }
 
-// ---------------------------------------------------------------------------
-// 128x128 tile of X, written both as 1x128 groups (rows) and as 128x1
-// groups (columns, stored transposed).  Thread t owns 8 consecutive rows
-// (8*(t/16) ..) of one 8-column chunk (t%16), loaded as 8 coalesced 16-byte
-// vectors; rows reduce across the 16 threads of a half-warp, columns across
-// the 16 row groups (shuffle, then shared memory).
-__global__ void __launch_bounds__(256) quant_act_dual_kernel(const uint16_t* __restrict__ x, int64_t M, int nkb,
-                                                              int64_t ldx, uint8_t* __restrict__ xq,
-                                                              float* __restrict__ sx, uint8_t* __restrict__ xq_t,
-                                                              float* __restrict__ sx_t) {
-  __shared__ float red[8][kGroup];
-  __shared__ float scol[kGroup];
-  const int t = threadIdx.x;
-  const int c = t & 15;
-  const int g = t >> 4;
-  const int warp = t >> 5;
-  const int64_t K = static_cast<int64_t>(nkb) * kGroup;
-  const int64_t rb = blockIdx.x / nkb;
-  const int64_t kb = blockIdx.x - rb * nkb;
-  const int64_t r0 = rb * kGroup + 8 * g;
-  const int64_t c0 = kb * kGroup + 8 * c;
+__device__ int g_quant_status;
 
-  uint4 v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = ld_stream_16(x + (r0 + j) * ldx + c0);
+// Barrier over the 256 compute threads (named barrier 1; the producer warp
+// never takes part) returning the AND of `v` over them.
+__device__ __forceinline__ bool compute_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
 
-  // 1x128 groups: one per row.
+__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// |x| maxima of the two halves of a packed BF16 pair, in both halves.
+__device__ __forceinline__ uint32_t umax_halves(uint32_t m) { return umax16x2(m, __byte_perm(m, 0u, 0x1032)); }
+
+// Row layout: quantises the thread's 64 values (32 words in load order) with
+// one divisor, stores the 64 codes, then fixes the value pairs whose bracket
+// was inconclusive with IEEE divisions (about 0.4% of values: each lane
+// walks its own flagged pairs after the bulk store, instead of every lane
+// of a warp stepping through every lane's fix-ups).
+__device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divisor& d, int h, const uint8_t* rowp,
+                                            int rsw, uint8_t* out) {
+  if (!d.fast) {
+    // s == 0 (all-zero group) or a subnormal s: exact path for every value
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float a = absmax8(v[j]);
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    const Divisor d = make_divisor(a);
-    bool bad = false;
-    const uint2 q = quant8(v[j], d, bad);
-    uint8_t* o = xq + (r0 + j) * K + c0;
-    *reinterpret_cast<uint2*>(o) = q;
-    if (bad) *reinterpret_cast<uint2*>(o) = quant_row8_exact(x + (r0 + j) * ldx + c0, d.s);
-    if (c == 0) sx[kb * M + r0 + j] = d.s;
+    for (int i = 0; i < 8; ++i) {
+      const int j = (i + 4 * h) & 7;
+      uint2 c;
+      c.x = quant2_exact(w[4 * i], d.s) | (quant2_exact(w[4 * i + 1], d.s) << 16);
+      c.y = quant2_exact(w[4 * i + 2], d.s) | (quant2_exact(w[4 * i + 3], d.s) << 16);
+      *reinterpret_cast<uint2*>(out + 8 * j) = c;
+    }
+    return;
   }
-
-  // 128x1 groups: one per column.
+  const float2 rlo = make_float2(d.r_lo, d.r_lo), rhi = make_float2(d.r_hi, d.r_hi);
+  uint2 cc[8];
+  uint32_t bm = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float a = 0.0f;
+    uint32_t lo[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a = fmaxf(a, __uint_as_float((col16(v[j], i) & 0x7FFFu) << 16));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
-    if ((t & 16) == 0) red[warp][8 * c + i] = a;
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t aw = w[4 * i + k] & 0x7FFF7FFFu;
+      const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
+      const float2 l = __fmul2_rd(a, rlo);
+      const float2 u = __fmul2_ru(a, rhi);
+      lo[k] = e4m3x2(l.x, l.y);
+      bm |= (lo[k] != e4m3x2(u.x, u.y)) ? (1u << (4 * i + k)) : 0u;
+    }
+    const uint32_t s0 = __byte_perm(w[4 * i], w[4 * i + 1], 0x7531) & 0x80808080u;
+    const uint32_t s1 = __byte_perm(w[4 * i + 2], w[4 * i + 3], 0x7531) & 0x80808080u;
+    cc[i] = make_uint2(__byte_perm(lo[0], lo[1], 0x5410) | s0, __byte_perm(lo[2], lo[3], 0x5410) | s1);
   }
-  __syncthreads();
-  if (t < kGroup) {
-    float a = red[0][t];
+  // load order -> column order: the upper half started at chunk 4
 #pragma unroll
-    for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
-    scol[t] = a;
-    sx_t[rb * K + kb * kGroup + t] = __fdiv_rn(a, kE4M3Max);
+  for (int i = 0; i < 4; ++i) {
+    const uint2 a = cc[i], b = cc[i + 4];
+    cc[i] = h ? b : a;
+    cc[i + 4] = h ? a : b;
   }
-  __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const Divisor d = make_divisor(scol[8 * c + i]);
-    bool bad = false;
-    const uint2 q = quant_col8(v, i, d, bad);
-    uint8_t* o = xq_t + (c0 + i) * M + r0;
-    *reinterpret_cast<uint2*>(o) = q;
-    if (bad) *reinterpret_cast<uint2*>(o) = quant_col8_exact(x + r0 * ldx + c0 + i, ldx, d.s);
+  for (int p = 0; p < 4; ++p)
+    *reinterpret_cast<uint4*>(out + 16 * p) = make_uint4(cc[2 * p].x, cc[2 * p].y, cc[2 * p + 1].x, cc[2 * p + 1].y);
+  while (bm != 0u) {
+    const int k = __ffs(bm) - 1;
+    bm &= bm - 1u;
+    const int j = ((k >> 2) + 4 * h) & 7;  // logical chunk of word k
+    const uint32_t wk = *reinterpret_cast<const uint32_t*>(rowp + (((j ^ rsw) << 4) | ((k & 3) << 2)));
+    *reinterpret_cast<uint16_t*>(out + 8 * j + 2 * (k & 3)) = static_cast<uint16_t>(quant2_exact(wk, d.s));
   }
 }
 
-// ---------------------------------------------------------------------------
-// One 128x128 weight block per CTA: the block's absmax is reduced over all
-// 256 threads, then every element is quantised with the one block scale.
-// Optionally also writes the transposed codes (Dgrad uses W transposed).
-__global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __restrict__ w, int nnb, int nkb,
-                                                            int64_t ldw, uint8_t* __restrict__ wq,
-                                                            float* __restrict__ sw, uint8_t* __restrict__ wq_t,
-                                                            float* __restrict__ sw_t) {
-  __shared__ float red[8];
-  const int t = threadIdx.x;
-  const int c = t & 15;
-  const int g = t >> 4;
-  const int64_t N = static_cast<int64_t>(nnb) * kGroup;
-  const int64_t K = static_cast<int64_t>(nkb) * kGroup;
-  const int64_t nb = blockIdx.x / nkb;
-  const int64_t kb = blockIdx.x - nb * nkb;
-  const int64_t r0 = nb * kGroup + 8 * g;
-  const int64_t c0 = kb * kGroup + 8 * c;
+template <int kMode>
+__global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileParams p) {
+  using Q = QCfg<kMode>;
+  extern __shared__ uint8_t qsmem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+  QShared& S = *reinterpret_cast<QShared*>(tiles + Q::kStages * kTileBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = p.nrb * p.nkb;
+  const int64_t K = static_cast<int64_t>(p.nkb) * kGroup;
 
-  uint4 v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = ld_stream_16(w + (r0 + j) * ldw + c0);
-  float a = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) a = fmaxf(a, absmax8(v[j]));
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  if ((t & 31) == 0) red[t >> 5] = a;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Q::kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kQComputeThreads / 32);  // one arrival per compute warp
+    }
+    fence_barrier_init();
+  }
+  div_table_init(S.tab);
   __syncthreads();
-  a = red[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-  const Divisor d = make_divisor(a);
-  if (t == 0) {
-    sw[nb * nkb + kb] = d.s;
-    if (sw_t != nullptr) sw_t[kb * nnb + nb] = d.s;
+
+  if (warp == kQComputeThreads / 32) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) prefetch_tmap(&tmx);
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    bool live = true;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      if (!__shfl_sync(0xffffffffu, mbar_wait(&S.empty[s], ph ^ 1u, p.timeout_ns), 0)) {
+        live = false;
+        break;
+      }
+      if (lane == 0) {
+        const int64_t rb = tile / p.nkb;
+        const int kb = static_cast<int>(tile - rb * p.nkb);
+        uint8_t* dst = tiles + s * kTileBytes;
+        mbar_arrive_expect_tx(&S.full[s], kTileBytes);
+        if (Q::kRowLayout) {
+          tma_load_2d(dst, &tmx, &S.full[s], kb * kGroup, static_cast<int>(rb * kGroup));
+          tma_load_2d(dst + kTileBytes / 2, &tmx, &S.full[s], kb * kGroup + kGroup / 2, static_cast<int>(rb * kGroup));
+        } else {
+          tma_load_2d(dst, &tmx, &S.full[s], kb * kGroup, static_cast<int>(rb * kGroup));
+        }
+      }
+      __syncwarp();
+      ++issued;
+      if (++s == Q::kStages) { s = 0; ph ^= 1u; }
+    }
+    if (!live) {
+      if (lane == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+      // the copies already issued land before the CTA may exit
+      for (int i = 0; i < Q::kStages && i < issued; ++i) {
+        int st = s - 1 - i;
+        uint32_t q = ph;
+        if (st < 0) { st += Q::kStages; q ^= 1u; }
+        (void)mbar_wait(&S.full[st], q, p.timeout_ns);
+      }
+    }
+    return;
   }
-  uint2 q[8];
-  uint32_t bad_rows = 0;
+
+  // ---------------------------------------------------------------- compute
+  const int t = threadIdx.x;
+  int s = 0;
+  uint32_t ph = 0, par = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, par ^= 1u) {
+    const int64_t rb = tile / p.nkb;
+    const int kb = static_cast<int>(tile - rb * p.nkb);
+    const bool ok = mbar_wait(&S.full[s], ph, p.timeout_ns);
+    const uint8_t* stage = tiles + s * kTileBytes;
+
+    if (Q::kRowLayout) {
+      const int r = t >> 1, h = t & 1, rsw = r & 7;
+      const uint8_t* rowp = stage + h * (kTileBytes / 2) + r * 128;
+      uint32_t w[32];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    bool bad = false;
-    q[j] = quant8(v[j], d, bad);
-    bad_rows |= bad ? (1u << j) : 0u;
-  }
-  if (bad_rows) {
+      for (int i = 0; i < 8; ++i) {
+        const int j = (i + 4 * h) & 7;
+        const uint4 v = ok ? *reinterpret_cast<const uint4*>(rowp + ((j ^ rsw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) m = umax16x2(m, w[k] & 0x7FFF7FFFu);
+      m = umax_halves(m);
+      m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the other half of the row
+      const int64_t row = rb * kGroup + r;
+      Divisor d;
+      if (kMode == kModeWeight) {
+#pragma unroll
+        for (int o = 2; o <= 16; o <<= 1) m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) S.red[par][warp] = m & 0xFFFFu;
+        if (!compute_bar_and(ok)) {
+          if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+          break;
+        }
+        uint32_t a = S.red[par][0];
+#pragma unroll
+        for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
+        d = table_divisor(S.tab, a);
+        if (t == 0) p.s[rb * p.nkb + kb] = d.s;
+      } else {
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+          break;
+        }
+        d = table_divisor(S.tab, m & 0xFFFFu);
+        if (h == 0 && row < p.rows) p.s[static_cast<int64_t>(kb) * p.rows + row] = d.s;
+      }
+      if (row < p.rows) quant_row64(w, d, h, rowp, rsw, p.q + row * K + static_cast<int64_t>(kb) * kGroup + 64 * h);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+      if (++s == Q::kStages) { s = 0; ph ^= 1u; }
+      continue;
+    }
+
+    // block layout
+    const int g = t >> 4;  // row group: rows 8g .. 8g+7 of the tile
+    const int c = t & 15;  // column chunk: columns 8c .. 8c+7 of the tile
+    uint4 v[8];
+    const uint8_t* src = stage + (8 * g) * kTileRowBytes + 16 * c;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (bad_rows & (1u << j)) q[j] = quant_row8_exact(w + (r0 + j) * ldw + c0, d.s);
-  }
+      v[j] = ok ? *reinterpret_cast<const uint4*>(src + j * kTileRowBytes) : make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (++s == Q::kStages) { s = 0; ph ^= 1u; }
+    const int64_t r0 = rb * kGroup + 8 * g;                        // this thread's first row
+    const int64_t c0 = static_cast<int64_t>(kb) * kGroup + 8 * c;  // and first column
+
+    if (kMode == kModeWeightT) {
+      uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(wq + (r0 + j) * K + c0) = q[j];
-  if (wq_t != nullptr) {
-    // One scale for the whole block, so the codes of W^T are the transposed
-    // codes of W: transpose this thread's 8x8 byte tile in registers.
+      for (int j = 0; j < 8; ++j) m = umax16x2(m, absmax8_bits(v[j]));
+      m = umax_halves(m) & 0xFFFFu;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(wq_t + (c0 + i) * N + r0) = byte_column(q, i);
+      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) S.red[par][warp] = m;
+      if (!compute_bar_and(ok)) {
+        if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+        break;
+      }
+      uint32_t a = S.red[par][0];
+#pragma unroll
+      for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
+      const Divisor d = table_divisor(S.tab, a);
+      if (t == 0) {
+        p.s[rb * p.nkb + kb] = d.s;
+        p.s_t[static_cast<int64_t>(kb) * p.nrb + rb] = d.s;
+      }
+      uint2 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t bm = 0;
+        q[j] = quant8m(v[j], d, bm);
+        if (bm) q[j] = fix8(q[j], v[j], d.s, bm);
+        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q[j];
+      }
+      // one scale for the block: the codes of W^T are the transposed codes
+#pragma unroll
+      for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = byte_column(q, i);
+      continue;
+    }
+
+    // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
+    // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
+    uint32_t am[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      am[i] = __byte_perm(umax_halves(absmax8_bits(v[2 * i])), umax_halves(absmax8_bits(v[2 * i + 1])), 0x5410);
+#pragma unroll
+      for (int o = 1; o <= 8; o <<= 1) am[i] = umax16x2(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
+    }
+    // 128x1 groups: column maxima over this thread's rows (two columns per
+    // word), then over the other row group of the warp
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t wd = k == 0 ? v[j].x : k == 1 ? v[j].y : k == 2 ? v[j].z : v[j].w;
+        m = umax16x2(m, wd & 0x7FFF7FFFu);
+      }
+      m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      if (lane < 16) S.colred[warp][4 * c + k] = m;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
+      const Divisor d = table_divisor(S.tab, a16);
+      uint32_t bm = 0;
+      uint2 q = quant8m(v[j], d, bm);
+      if (bm) q = fix8(q, v[j], d.s, bm);
+      *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q;
+      if (c == 0) p.s[static_cast<int64_t>(kb) * p.rows + r0 + j] = d.s;
+    }
+    if (!compute_bar_and(ok)) {
+      if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+      break;
+    }
+    if (t < kGroup / 2) {
+      uint32_t m = S.colred[0][t];
+#pragma unroll
+      for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t]);
+      S.colmax[t] = m;
+      float* st = p.s_t + rb * K + static_cast<int64_t>(kb) * kGroup + 2 * t;
+      st[0] = table_divisor(S.tab, m & 0xFFFFu).s;
+      st[1] = table_divisor(S.tab, m >> 16).s;
+    }
+    compute_bar();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t m = S.colmax[4 * c + (i >> 1)];
+      const Divisor d = table_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu));
+      bool bad = false;
+      uint2 q = quant_col8(v, i, d, bad);
+      if (bad) q = quant_col8_exact(v, i, d.s);
+      *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = q;
+    }
   }
+}
+
+// Tensor map of a BF16 matrix [rows][ld] (cols used): 128x128 boxes, or for
+// the row layout 128-row x 64-column boxes with 128-byte swizzling.
+bool encode_bf16_tiles(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t cols, int64_t ld,
+                       bool row_layout) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_layout ? kGroup / 2 : kGroup), static_cast<cuuint32_t>(kGroup)};
+  cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), gdim, gstride, box,
+                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         row_layout ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int kMode>
+cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int sm_count, cudaStream_t stream) {
+  const int64_t ntiles = p.nrb * p.nkb;
+  if (ntiles <= 0) return cudaSuccess;
+  CUtensorMap map;
+  if (!encode_bf16_tiles(&map, x, p.rows, static_cast<int64_t>(p.nkb) * kGroup, ld, QCfg<kMode>::kRowLayout))
+    return cudaErrorInvalidValue;
+  auto kern = quant_tile_kernel<kMode>;
+  constexpr int smem = q_smem_bytes<kMode>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  static int per_sm = 0;  // co-resident CTAs per SM
+  if (per_sm == 0) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kQThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+  const int grid = static_cast<int>(ntiles < slots ? ntiles : slots);
+  kern<<<grid, kQThreads, smem, stream>>>(map, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                      float* sx, int sm_count, cudaStream_t stream) {
-  const int nkb = static_cast<int>(K / kGroup);
-  const int64_t n16 = M * nkb * 8;
-  if (n16 >= (int64_t(1) << 34)) return cudaErrorInvalidValue;  // group index must fit 31 bits
-  // ceil(2^40 / nkb): the multiply-high division is exact for nkb < 512
-  const uint64_t magic = nkb < 512 ? ((uint64_t(1) << 40) + nkb - 1) / nkb : 0;
-  static int per_sm = 0;  // resident 256-thread blocks per SM
-  if (per_sm == 0) {
-    int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_act_1x128_kernel, 256, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
-  const int64_t blocks_needed = (n16 + 255) / 256;
-  const int64_t max_blocks = static_cast<int64_t>(sm_count) * per_sm;
-  const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-  if (blocks <= 0) return cudaSuccess;
-  quant_act_1x128_kernel<<<blocks, 256, 0, stream>>>(x, M, nkb, ldx, magic, xq, sx);
-  return cudaGetLastError();
+                                      float* sx, int sm_count, uint64_t timeout_ns, cudaStream_t stream) {
+  const TileParams p{M, (M + kGroup - 1) / kGroup, static_cast<int>(K / kGroup), xq, sx, nullptr, nullptr, timeout_ns};
+  return launch_tiles<kModeAct>(x, ldx, p, sm_count, stream);
 }
 
 cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                     float* sx, uint8_t* xq_t, float* sx_t, cudaStream_t stream) {
-  const int nkb = static_cast<int>(K / kGroup);
-  const int64_t tiles = (M / kGroup) * nkb;
-  if (tiles <= 0) return cudaSuccess;
-  quant_act_dual_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(x, M, nkb, ldx, xq, sx, xq_t, sx_t);
-  return cudaGetLastError();
+                                     float* sx, uint8_t* xq_t, float* sx_t, int sm_count, uint64_t timeout_ns,
+                                     cudaStream_t stream) {
+  const TileParams p{M, M / kGroup, static_cast<int>(K / kGroup), xq, sx, xq_t, sx_t, timeout_ns};
+  return launch_tiles<kModeDual>(x, ldx, p, sm_count, stream);
 }
 
 cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
-                                   float* sw, uint8_t* wq_t, float* sw_t, cudaStream_t stream) {
-  const int nnb = static_cast<int>(N / kGroup);
-  const int nkb = static_cast<int>(K / kGroup);
-  const int64_t tiles = static_cast<int64_t>(nnb) * nkb;
-  if (tiles <= 0) return cudaSuccess;
-  quant_weight_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(w, nnb, nkb, ldw, wq, sw, wq_t, sw_t);
-  return cudaGetLastError();
+                                   float* sw, uint8_t* wq_t, float* sw_t, int sm_count, uint64_t timeout_ns,
+                                   cudaStream_t stream) {
+  const TileParams p{N, N / kGroup, static_cast<int>(K / kGroup), wq, sw, wq_t, sw_t, timeout_ns};
+  if (wq_t != nullptr) return launch_tiles<kModeWeightT>(w, ldw, p, sm_count, stream);
+  return launch_tiles<kModeWeight>(w, ldw, p, sm_count, stream);
+}
+
+cudaError_t quant_take_status(int* status) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(int));
+  }
+  *status = v;
+  return e;
 }
 
 }  // namespace fp8bs
