@@ -129,6 +129,15 @@ __device__ __forceinline__ void fold_row(float2* acc, const uint32_t (&p)[32], f
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_status, 0, code); }
 
+// A bounded mbarrier wait made by a whole warp, with lane 0's outcome.  The
+// producer and MMA-issuer warps run their loops converged (lane 0 issues
+// the copies and MMAs): a warp whose lane 0 loops alone while its other
+// lanes wait at the final CTA barrier slowed the epilogue warps sharing its
+// SM sub-partition.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  return __shfl_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns), 0);
+}
+
 // Tile t -> (first row, first column, group).  Tiles run m-tile-major with
 // the BN-wide n-tiles of one m-tile consecutive, so concurrently running
 // CTAs share A rows.
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kEpiWarp0) {
     setmaxnreg_dec<kRegsProducer>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ---------------------------------------------------------- producer
       int stage = 0;
       uint32_t phase = 0;
@@ -269,26 +278,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         int row0, n0, g;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
         for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
-          if (kPair) {
-            // Both CTAs' tiles complete on the leader's barrier, which the
-            // leader arms for the pair's bytes; each CTA loads its A rows
-            // and its half of the B tile into its own shared memory.
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (C::kABytes + C::kBBytes));
-            const uint32_t leader_full = mapa_shared(&full[stage], 0);
-            tma_load_2d_pair(sA + stage * C::kABytes, &tmA, leader_full, kb * kBlockK, row0);
-            tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
-                             n0 + static_cast<int>(rank) * (BN / 2));
-            ++issued;
-            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-            continue;
+          if (!warp_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
+          if (lane == 0) {
+            if (kPair) {
+              // Both CTAs' tiles complete on the leader's barrier, which the
+              // leader arms for the pair's bytes; each CTA loads its A rows
+              // and its half of the B tile into its own shared memory.
+              if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (C::kABytes + C::kBBytes));
+              const uint32_t leader_full = mapa_shared(&full[stage], 0);
+              tma_load_2d_pair(sA + stage * C::kABytes, &tmA, leader_full, kb * kBlockK, row0);
+              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
+                               n0 + static_cast<int>(rank) * (BN / 2));
+            } else {
+              mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
+              tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBlockK, row0);
+              if (kGrouped)
+                tma_load_3d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0, g);
+              else
+                tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0);
+            }
           }
-          mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
-          tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBlockK, row0);
-          if (kGrouped)
-            tma_load_3d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0, g);
-          else
-            tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBlockK, n0);
+          __syncwarp();
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
@@ -304,13 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           (void)mbar_wait(&full[st], ph, p.timeout_ns);
         }
       }
-    } else if ((warp == 1 || warp == 3) && lane == 0 && rank == 0) {
+    } else if ((warp == 1 || warp == 3) && rank == 0) {
       // --------------------------------------------------------- MMA issuers
-      // Two issuing threads take alternate k-block steps (warp 1 the even
-      // ones, warp 3 the odd ones): issuing a k-block's MMAs blocks the
-      // issuing thread for about as long as the tensor core takes to
-      // accept them, so one thread can prepare the next step while the
-      // other's MMAs drain.  Step s uses TMEM buffer s % kBufs.  With pairs
+      // Two issuing warps take alternate k-block steps (warp 1 the even
+      // ones, warp 3 the odd ones; lane 0 issues): issuing a k-block's MMAs
+      // blocks the issuing thread for about as long as the tensor core
+      // takes to accept them, so one warp can prepare the next step while
+      // the other's MMAs drain.  Step s uses TMEM buffer s % kBufs.  With pairs
       // only the leader CTA issues: one M=256 MMA covers both CTAs.
       constexpr uint32_t idesc = idesc_e4m3_f32(kPair ? 2 * kBlockM : kBlockM, BN);
       const uint32_t parity = warp == 1 ? 0u : 1u;
@@ -323,36 +333,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t phase = (step / C::kStages) & 1u;
           const uint32_t buf = step % C::kBufs;
           const uint32_t tphase = (step / C::kBufs) & 1u;
-          if (!mbar_wait(&full[stage], phase, p.timeout_ns)) { live = false; break; }
-          if (!mbar_wait(&t_empty[buf], tphase ^ 1, p.timeout_ns)) { live = false; break; }
+          if (!warp_wait(&full[stage], phase, p.timeout_ns)) { live = false; break; }
+          if (!warp_wait(&t_empty[buf], tphase ^ 1, p.timeout_ns)) { live = false; break; }
           tc_fence_after_sync();
-          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
-          const uint32_t dtmem = tmem_base + buf * BN;
-          if (kPair) {
+          if (lane == 0) {
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+            const uint32_t dtmem = tmem_base + buf * BN;
+            if (kPair) {
 #pragma unroll
-            for (int k = 0; k < kBlockK / kUmmaK; ++k)
-              mma_e4m3_pair(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-            mma_commit_pair(&empty[stage], 0x3);
-            mma_commit_pair(&t_full[buf], 0x3);
-          } else {
+              for (int k = 0; k < kBlockK / kUmmaK; ++k)
+                mma_e4m3_pair(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+              mma_commit_pair(&empty[stage], 0x3);
+              mma_commit_pair(&t_full[buf], 0x3);
+            } else {
 #pragma unroll
-            for (int k = 0; k < kBlockK / kUmmaK; ++k)
-              mma_e4m3(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-            mma_commit(&empty[stage]);
-            mma_commit(&t_full[buf]);
+              for (int k = 0; k < kBlockK / kUmmaK; ++k)
+                mma_e4m3(dtmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+              mma_commit(&empty[stage]);
+              mma_commit(&t_full[buf]);
+            }
           }
+          __syncwarp();
         }
       }
       if (!live) {
         record_status(kStatusTimeout);
         *abort_flag = 1;
       }
-      // wait for every MMA this thread issued before TMEM can be released
-      if (kPair)
-        mma_commit_pair(&teardown[parity], 0x1);
-      else
-        mma_commit(&teardown[parity]);
+      // wait for every MMA this warp issued before TMEM can be released
+      if (lane == 0) {
+        if (kPair)
+          mma_commit_pair(&teardown[parity], 0x1);
+        else
+          mma_commit(&teardown[parity]);
+      }
+      __syncwarp();
       (void)mbar_wait(&teardown[parity], 0, p.timeout_ns);
     } else if (warp == 2) {
       // ----------------------------------------------------- scale loader

@@ -6,8 +6,8 @@
 // s = fl32(absmax / 448) and code = E4M3_rne_satfinite(fl32(x / s)), both
 // quotients IEEE round-to-nearest; a group with s == 0 gets all-zero codes.
 // The per-element quotient is decided from a two-sided bracket of x * (1/s)
-// (quant2 below), so the kernels stay HBM-bound streaming kernels: every
-// byte is read once and written once, with coalesced 16-byte loads.
+// (quant8m below) with IEEE divisions only where the bracket is
+// inconclusive, so every byte is read once and written once.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -22,13 +22,24 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Per-group divisor s and a bracket [r_lo, r_hi] of 1/s (both float32).
+// Per-group divisor s with two reciprocals bracketing 1/s:
+//   r_lo = RD(1/s) <= 1/s,   r_up = RU(1/s) + 2 ulps,
+// where r_up is far enough above 1/s that a product truncated toward zero
+// still bounds the quotient: |RZ(x * r_up)| >= |x| / s.  (Truncation loses
+// less than 2^-23 of the product, the two extra ulps add at least 2^-23.)
 struct Divisor {
   float s;
-  float r_lo, r_hi;
-  uint64_t r_lo2, r_hi2;  // {r_lo, r_lo} and {r_hi, r_hi} for packed FP32x2 multiplies
+  float r_lo, r_up;
   bool fast;  // s is a normal float32; s == 0 and subnormal s take the exact path
 };
+
+// RU(1/s) + 2 ulps from r_lo = RD(1/s): RU(1/s) is r_lo itself when 1/s is
+// exact (r_lo * s == 1, tested exactly by one fused multiply-add), else the
+// next float up.
+__device__ __forceinline__ float recip_up(float r_lo, float s) {
+  const uint32_t b = __float_as_uint(r_lo) + ((fmaf(r_lo, s, -1.0f) == 0.0f) ? 0u : 1u);
+  return __uint_as_float(b + 2u);
+}
 
 __device__ __forceinline__ Divisor make_divisor(float absmax) {
   Divisor d;
@@ -36,11 +47,7 @@ __device__ __forceinline__ Divisor make_divisor(float absmax) {
   d.fast = d.s >= 1.17549435e-38f;    // FLT_MIN: 1/s is then a finite normal float
   const float s = d.fast ? d.s : 1.0f;
   d.r_lo = __frcp_rd(s);              // r_lo <= 1/s
-  // r_hi >= 1/s: r_lo itself when 1/s is exact (r_lo * s == 1, tested
-  // exactly by one fused multiply-add), else the next float up.
-  d.r_hi = (fmaf(d.r_lo, s, -1.0f) == 0.0f) ? d.r_lo : __uint_as_float(__float_as_uint(d.r_lo) + 1u);
-  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_lo2) : "f"(d.r_lo));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_hi2) : "f"(d.r_hi));
+  d.r_up = recip_up(d.r_lo, s);
   return d;
 }
 
@@ -48,24 +55,23 @@ __device__ __forceinline__ Divisor make_divisor(float absmax) {
 // scale is s = fl32(a / 448) = fl32((1 + f/128) / 448) * 2^e exactly, and
 // the reciprocal brackets scale by 2^-e in the same way (scaling by a power
 // of two commutes with rounding while everything stays normal).  So the
-// 128 values fl32((1 + f/128) / 448), their RD reciprocals and the RU
-// reciprocals are computed once per block with the IEEE intrinsics and the
-// per-group work is an exponent add.  Zero, subnormal or huge absmax values
-// take make_divisor.
+// 128 values fl32((1 + f/128) / 448) and their reciprocal brackets are
+// computed once per block with the IEEE intrinsics and the per-group work
+// is an exponent add.  Zero, subnormal or huge absmax values take
+// make_divisor.
 struct DivTable {
   uint32_t s[128];     // bits of fl32((1 + f/128) / 448)
   uint32_t rlo[128];   // bits of RD(1 / s)
-  uint32_t rhi[128];   // bits of RU(1 / s)
+  uint32_t rup[128];   // bits of RU(1 / s) + 2 ulps
 };
 
 __device__ __forceinline__ void div_table_init(DivTable& t) {
   for (int f = threadIdx.x; f < 128; f += blockDim.x) {
     const float sf = __fdiv_rn(1.0f + static_cast<float>(f) * (1.0f / 128.0f), kE4M3Max);
     const float lo = __frcp_rd(sf);
-    const float hi = (fmaf(lo, sf, -1.0f) == 0.0f) ? lo : __uint_as_float(__float_as_uint(lo) + 1u);
     t.s[f] = __float_as_uint(sf);
     t.rlo[f] = __float_as_uint(lo);
-    t.rhi[f] = __float_as_uint(hi);
+    t.rup[f] = __float_as_uint(recip_up(lo, sf));
   }
 }
 
@@ -80,31 +86,9 @@ __device__ __forceinline__ Divisor table_divisor(const DivTable& t, uint32_t a16
   Divisor d;
   d.s = __uint_as_float(t.s[f] + (static_cast<uint32_t>(sh) << 23));
   d.r_lo = __uint_as_float(t.rlo[f] - (static_cast<uint32_t>(sh) << 23));
-  d.r_hi = __uint_as_float(t.rhi[f] - (static_cast<uint32_t>(sh) << 23));
+  d.r_up = __uint_as_float(t.rup[f] - (static_cast<uint32_t>(sh) << 23));
   d.fast = true;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_lo2) : "f"(d.r_lo));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(d.r_hi2) : "f"(d.r_hi));
   return d;
-}
-
-// E4M3 codes of fl32(x0 / s) and fl32(x1 / s) for the two BF16 values of
-// `w` (x0 in the low half), without a division per element:
-//   lo = RD(|x| * r_lo) <= |x| / s <= RU(|x| * r_hi) = hi,
-// so the correctly rounded quotient fl32(|x| / s) lies in [lo, hi] too.
-// Rounding to E4M3 (RNE, saturating) is monotonic, hence when lo and hi
-// round to the same codes, so does fl32(|x| / s).  When an E4M3 rounding
-// boundary falls inside the 2-3 ulp wide bracket (rare), or s is not a
-// normal float, `bad` is set and the caller redoes the chunk with IEEE
-// divisions (quant8_exact).  The sign is applied last: the quotient has
-// x's sign, also for -0 and for results that round to zero.
-__device__ __forceinline__ uint32_t quant2(uint32_t w, const Divisor& d, bool& bad) {
-  const uint32_t aw = w & 0x7FFF7FFFu;
-  const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
-  const float2 l = __fmul2_rd(a, make_float2(d.r_lo, d.r_lo));
-  const float2 h = __fmul2_ru(a, make_float2(d.r_hi, d.r_hi));
-  const uint32_t c = e4m3x2(l.x, l.y);
-  bad |= (c != e4m3x2(h.x, h.y));
-  return c | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
 }
 
 // Largest |x| of BF16 values: for non-negative floats the integer order of
@@ -116,42 +100,51 @@ __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Running |x| maximum of BF16 pairs, one instruction per word: the
+// magnitude of max.xorsign.abs is max(|a|, |b|); its sign bit is junk that
+// abs_bits clears once at the end.
+__device__ __forceinline__ uint32_t absmax_step(uint32_t m, uint32_t w) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(m), "r"(w));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t abs_bits(uint32_t m) { return m & 0x7FFF7FFFu; }
+
 __device__ __forceinline__ uint32_t absmax8_bits(uint4 v) {
-  const uint32_t k = 0x7FFF7FFFu;
-  return umax16x2(umax16x2(v.x & k, v.y & k), umax16x2(v.z & k, v.w & k));
+  return abs_bits(absmax_step(absmax_step(v.x, v.y), absmax_step(v.z, v.w)));
 }
 
-// Packed |bf16| maximum -> float32.
-__device__ __forceinline__ float absmax_to_f32(uint32_t m) {
-  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+// Eight consecutive values of one group -> eight codes (byte i = value i),
+// without a division per element.  With signed products truncated toward
+// zero,
+//   |RZ(x * r_lo)| <= |x| / s <= |RZ(x * r_up)|,
+// both of x's sign, so the correctly rounded quotient fl32(x / s) lies
+// between them.  Rounding to E4M3 (RNE, saturating) is monotonic and odd,
+// hence when both ends give the same code (sign included), so does
+// fl32(x / s).  When an E4M3 rounding boundary falls inside the few-ulp
+// wide bracket, or s is not a normal float, bit j of `badmask` is set for
+// the pair (values 2j, 2j+1) and the caller redoes it with quant2_exact.
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float2 rlo, float2 rup, uint32_t& bad) {
+  const float2 a = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  const float2 l = __fmul2_rz(a, rlo);
+  const float2 u = __fmul2_rz(a, rup);
+  const uint32_t c = e4m3x2(l.x, l.y);
+  bad = c != e4m3x2(u.x, u.y) ? 1u : 0u;
+  return c;
 }
 
-__device__ __forceinline__ float absmax8(uint4 v) { return absmax_to_f32(absmax8_bits(v)); }
-
-// Eight consecutive values -> eight codes (byte i = value i).  The code
-// pairs of both brackets are packed and compared; the sign bits of the
-// inputs are gathered with one byte permute per word pair.  Bit j of
-// `badmask` is set when pair j (values 2j, 2j+1) needs the exact path.
 __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& badmask) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const float2 rlo = make_float2(d.r_lo, d.r_lo), rhi = make_float2(d.r_hi, d.r_hi);
-  uint32_t lo[4], hi[4];
+  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
+  uint32_t c[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    // |x| of both halves as float32, times the brackets with rounding down
-    // and up (packed FP32x2 multiplies)
-    const uint32_t aw = w[j] & 0x7FFF7FFFu;
-    const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
-    const float2 l = __fmul2_rd(a, rlo);
-    const float2 h = __fmul2_ru(a, rhi);
-    lo[j] = e4m3x2(l.x, l.y);
-    hi[j] = e4m3x2(h.x, h.y);
-    badmask |= (lo[j] != hi[j] || !d.fast) ? (1u << j) : 0u;
+    uint32_t b;
+    c[j] = quant_pair(w[j], rlo, rup, b);
+    badmask |= (b | (d.fast ? 0u : 1u)) << j;
   }
-  const uint32_t s0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
-  const uint32_t s1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
-  const uint32_t c0 = __byte_perm(lo[0], lo[1], 0x5410), c1 = __byte_perm(lo[2], lo[3], 0x5410);
-  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(c0 | s0, c1 | s1);
+  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
 }
 
 // Codes of one value pair through IEEE divisions (x / s, then E4M3, sign
@@ -162,43 +155,6 @@ __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& ba
 __device__ __forceinline__ uint32_t quant2_exact(uint32_t w, float s) {
   if (s == 0.0f) return 0u;
   return e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
-}
-
-// Patches the pairs flagged in `badmask` of an 8-code chunk.
-__device__ __forceinline__ uint2 fix8(uint2 q, uint4 v, float s, uint32_t badmask) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[2] = {q.x, q.y};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (badmask & (1u << j)) {
-      const uint32_t e = quant2_exact(w[j], s);
-      const int sh = 16 * (j & 1);
-      c[j >> 1] = (c[j >> 1] & ~(0xFFFFu << sh)) | (e << sh);
-    }
-  }
-  return make_uint2(c[0], c[1]);
-}
-
-// The same codes through IEEE divisions, x / s then E4M3 (the fix-up path).
-__device__ __forceinline__ uint32_t quant1_exact(uint32_t h, float s) {
-  if (s == 0.0f) return 0u;
-  const float q = __fdiv_rn(__uint_as_float(h << 16), s);
-  return e4m3x2(q, 0.0f) & 0xFFu;
-}
-
-// BF16 bits of column i (0..7) of an 8-value row chunk.
-__device__ __forceinline__ uint32_t col16(const uint4& v, int i) {
-  const uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
-  return (i & 1) ? (w >> 16) : (w & 0xFFFFu);
-}
-
-// Codes of column i of rows 0..7 (one byte per row, row 0 lowest).
-__device__ __forceinline__ uint2 quant_col8(const uint4 (&v)[8], int i, const Divisor& d, bool& bad) {
-  bad |= !d.fast;
-  uint32_t p[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) p[j] = quant2(col16(v[2 * j], i) | (col16(v[2 * j + 1], i) << 16), d, bad);
-  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
 // Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
@@ -215,15 +171,6 @@ __device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
     p[j] = __byte_perm(x0, x1, sel);
   }
   return make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
-}
-
-// Exact codes of column i of rows 0..7 through IEEE divisions (the fix-up
-// path of quant_col8).
-__device__ __noinline__ uint2 quant_col8_exact(const uint4 (&v)[8], int i, float s) {
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = quant1_exact(col16(v[j], i), s);
-  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
 // ---------------------------------------------------------------------------
@@ -257,15 +204,15 @@ enum TileMode : int {
 template <int kMode>
 struct QCfg {
   static constexpr bool kRowLayout = kMode == kModeAct || kMode == kModeWeight;
-  static constexpr int kStages = kRowLayout ? 3 : 4;
-  static constexpr int kMinBlocks = kRowLayout ? 2 : 1;  // CTAs per SM the registers are budgeted for
+  static constexpr int kStages = 3;
+  static constexpr int kMinBlocks = 2;  // CTAs per SM the registers and shared memory are budgeted for
 };
 
 constexpr int kQComputeThreads = 256;
 constexpr int kQThreads = kQComputeThreads + 32;  // + the producer warp
 constexpr int kTileBytes = kGroup * kGroup * 2;    // 32 KB of BF16
 constexpr int kTileRowBytes = kGroup * 2;
-constexpr int kQMaxStages = 4;
+constexpr int kQMaxStages = 3;
 
 struct TileParams {
   int64_t rows;     // rows of the input (M, or N for a weight)
@@ -285,6 +232,7 @@ struct QShared {
   uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
   uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
   uint32_t colmax[kGroup / 2];                         // dual: column maxima of the tile, two per word
+  uint32_t rowabs[kGroup];                             // dual: row maxima of the tile (BF16 bits)
 };
 
 template <int kMode>
@@ -333,24 +281,19 @@ __device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divis
     }
     return;
   }
-  const float2 rlo = make_float2(d.r_lo, d.r_lo), rhi = make_float2(d.r_hi, d.r_hi);
+  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
   uint2 cc[8];
   uint32_t bm = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t lo[4];
+    uint32_t c[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t aw = w[4 * i + k] & 0x7FFF7FFFu;
-      const float2 a = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
-      const float2 l = __fmul2_rd(a, rlo);
-      const float2 u = __fmul2_ru(a, rhi);
-      lo[k] = e4m3x2(l.x, l.y);
-      bm |= (lo[k] != e4m3x2(u.x, u.y)) ? (1u << (4 * i + k)) : 0u;
+      uint32_t b;
+      c[k] = quant_pair(w[4 * i + k], rlo, rup, b);
+      bm |= b << (4 * i + k);
     }
-    const uint32_t s0 = __byte_perm(w[4 * i], w[4 * i + 1], 0x7531) & 0x80808080u;
-    const uint32_t s1 = __byte_perm(w[4 * i + 2], w[4 * i + 3], 0x7531) & 0x80808080u;
-    cc[i] = make_uint2(__byte_perm(lo[0], lo[1], 0x5410) | s0, __byte_perm(lo[2], lo[3], 0x5410) | s1);
+    cc[i] = make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
   }
   // load order -> column order: the upper half started at chunk 4
 #pragma unroll
@@ -457,10 +400,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
       }
-      uint32_t m = 0;
+      uint32_t m = w[0];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) m = umax16x2(m, w[k] & 0x7FFF7FFFu);
-      m = umax_halves(m);
+      for (int k = 1; k < 32; ++k) m = absmax_step(m, w[k]);
+      m = umax_halves(abs_bits(m));
       m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the other half of the row
       const int64_t row = rb * kGroup + r;
       Divisor d;
@@ -495,16 +438,14 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
     // block layout
     const int g = t >> 4;  // row group: rows 8g .. 8g+7 of the tile
     const int c = t & 15;  // column chunk: columns 8c .. 8c+7 of the tile
-    uint4 v[8];
     const uint8_t* src = stage + (8 * g) * kTileRowBytes + 16 * c;
+    uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       v[j] = ok ? *reinterpret_cast<const uint4*>(src + j * kTileRowBytes) : make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
-    if (++s == Q::kStages) { s = 0; ph ^= 1u; }
     const int64_t r0 = rb * kGroup + 8 * g;                        // this thread's first row
     const int64_t c0 = static_cast<int64_t>(kb) * kGroup + 8 * c;  // and first column
+    uint32_t rowbad = 0;  // bit 4j+k: pair k of row j needs the exact path
 
     if (kMode == kModeWeightT) {
       uint32_t m = 0;
@@ -531,70 +472,119 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       for (int j = 0; j < 8; ++j) {
         uint32_t bm = 0;
         q[j] = quant8m(v[j], d, bm);
-        if (bm) q[j] = fix8(q[j], v[j], d.s, bm);
+        rowbad |= bm << (4 * j);
         *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q[j];
       }
       // one scale for the block: the codes of W^T are the transposed codes
 #pragma unroll
       for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = byte_column(q, i);
-      continue;
-    }
-
-    // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
-    // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
-    uint32_t am[4];
+      while (rowbad != 0u) {
+        const int b = __ffs(rowbad) - 1;
+        rowbad &= rowbad - 1u;
+        const int j = b >> 2, k = b & 3;
+        const uint32_t e = quant2_exact(*reinterpret_cast<const uint32_t*>(src + j * kTileRowBytes + 4 * k), d.s);
+        *reinterpret_cast<uint16_t*>(p.q + (r0 + j) * K + c0 + 2 * k) = static_cast<uint16_t>(e);
+        p.q_t[(c0 + 2 * k) * p.rows + r0 + j] = static_cast<uint8_t>(e);
+        p.q_t[(c0 + 2 * k + 1) * p.rows + r0 + j] = static_cast<uint8_t>(e >> 8);
+      }
+    } else {
+      // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
+      // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
+      uint32_t am[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      am[i] = __byte_perm(umax_halves(absmax8_bits(v[2 * i])), umax_halves(absmax8_bits(v[2 * i + 1])), 0x5410);
+      for (int i = 0; i < 4; ++i) {
+        am[i] = __byte_perm(umax_halves(absmax8_bits(v[2 * i])), umax_halves(absmax8_bits(v[2 * i + 1])), 0x5410);
 #pragma unroll
-      for (int o = 1; o <= 8; o <<= 1) am[i] = umax16x2(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
-    }
-    // 128x1 groups: column maxima over this thread's rows (two columns per
-    // word), then over the other row group of the warp
+        for (int o = 1; o <= 8; o <<= 1) am[i] = umax16x2(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
+      }
+      if (c == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t m = 0;
+        for (int i = 0; i < 4; ++i) {
+          S.rowabs[8 * g + 2 * i] = am[i] & 0xFFFFu;
+          S.rowabs[8 * g + 2 * i + 1] = am[i] >> 16;
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t wd = k == 0 ? v[j].x : k == 1 ? v[j].y : k == 2 ? v[j].z : v[j].w;
-        m = umax16x2(m, wd & 0x7FFF7FFFu);
+        const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
+        const Divisor d = table_divisor(S.tab, a16);
+        uint32_t bm = 0;
+        const uint2 q = quant8m(v[j], d, bm);
+        rowbad |= bm << (4 * j);
+        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q;
+        if (c == 0) p.s[static_cast<int64_t>(kb) * p.rows + r0 + j] = d.s;
       }
-      m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      if (lane < 16) S.colred[warp][4 * c + k] = m;
-    }
+      // 128x1 groups: transpose the 8x8 sub-block (column i of the tile
+      // chunk becomes vector i: rows 8g .. 8g+7 of that column), reduce the
+      // column maxima over the 16 row groups, then quantise every column
+      // vector like a row chunk; its 8 codes are 8 consecutive bytes of X^T.
+      uint4 vt[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
-      const Divisor d = table_divisor(S.tab, a16);
-      uint32_t bm = 0;
-      uint2 q = quant8m(v[j], d, bm);
-      if (bm) q = fix8(q, v[j], d.s, bm);
-      *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q;
-      if (c == 0) p.s[static_cast<int64_t>(kb) * p.rows + r0 + j] = d.s;
-    }
-    if (!compute_bar_and(ok)) {
-      if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
-      break;
-    }
-    if (t < kGroup / 2) {
-      uint32_t m = S.colred[0][t];
+      for (int k = 0; k < 4; ++k) {
+        uint32_t lo[4], hi[4];
 #pragma unroll
-      for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t]);
-      S.colmax[t] = m;
-      float* st = p.s_t + rb * K + static_cast<int64_t>(kb) * kGroup + 2 * t;
-      st[0] = table_divisor(S.tab, m & 0xFFFFu).s;
-      st[1] = table_divisor(S.tab, m >> 16).s;
-    }
-    compute_bar();
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t a = k == 0 ? v[2 * m].x : k == 1 ? v[2 * m].y : k == 2 ? v[2 * m].z : v[2 * m].w;
+          const uint32_t b = k == 0 ? v[2 * m + 1].x : k == 1 ? v[2 * m + 1].y : k == 2 ? v[2 * m + 1].z : v[2 * m + 1].w;
+          lo[m] = __byte_perm(a, b, 0x5410);
+          hi[m] = __byte_perm(a, b, 0x7632);
+        }
+        vt[2 * k] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        vt[2 * k + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t m = S.colmax[4 * c + (i >> 1)];
-      const Divisor d = table_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu));
-      bool bad = false;
-      uint2 q = quant_col8(v, i, d, bad);
-      if (bad) q = quant_col8_exact(v, i, d.s);
-      *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = q;
+      for (int k = 0; k < 4; ++k) {
+        uint32_t m = __byte_perm(umax_halves(absmax8_bits(vt[2 * k])), umax_halves(absmax8_bits(vt[2 * k + 1])), 0x5410);
+        m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (lane < 16) S.colred[warp][4 * c + k] = m;
+      }
+      if (!compute_bar_and(ok)) {
+        if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
+        break;
+      }
+      if (t < kGroup / 2) {
+        uint32_t m = S.colred[0][t];
+#pragma unroll
+        for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t]);
+        S.colmax[t] = m;
+        float* st = p.s_t + rb * K + static_cast<int64_t>(kb) * kGroup + 2 * t;
+        st[0] = table_divisor(S.tab, m & 0xFFFFu).s;
+        st[1] = table_divisor(S.tab, m >> 16).s;
+      }
+      compute_bar();
+      uint32_t colbad = 0;  // bit 4i+m: rows 2m, 2m+1 of column i need the exact path
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t m = S.colmax[4 * c + (i >> 1)];
+        const Divisor d = table_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu));
+        uint32_t bm = 0;
+        const uint2 q = quant8m(vt[i], d, bm);
+        colbad |= bm << (4 * i);
+        *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = q;
+      }
+      while (rowbad != 0u) {
+        const int b = __ffs(rowbad) - 1;
+        rowbad &= rowbad - 1u;
+        const int j = b >> 2, k = b & 3;
+        const float sj = table_divisor(S.tab, S.rowabs[8 * g + j]).s;
+        const uint32_t e = quant2_exact(*reinterpret_cast<const uint32_t*>(src + j * kTileRowBytes + 4 * k), sj);
+        *reinterpret_cast<uint16_t*>(p.q + (r0 + j) * K + c0 + 2 * k) = static_cast<uint16_t>(e);
+      }
+      while (colbad != 0u) {
+        const int b = __ffs(colbad) - 1;
+        colbad &= colbad - 1u;
+        const int i = b >> 2, m = b & 3;
+        const uint32_t cm = S.colmax[4 * c + (i >> 1)];
+        const float si = table_divisor(S.tab, (i & 1) ? (cm >> 16) : (cm & 0xFFFFu)).s;
+        const uint16_t* col = reinterpret_cast<const uint16_t*>(src + 2 * m * kTileRowBytes) + i;
+        const uint32_t wd = static_cast<uint32_t>(col[0]) | (static_cast<uint32_t>(col[kTileRowBytes / 2]) << 16);
+        *reinterpret_cast<uint16_t*>(p.q_t + (c0 + i) * p.rows + r0 + 2 * m) =
+            static_cast<uint16_t>(quant2_exact(wd, si));
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (++s == Q::kStages) { s = 0; ph ^= 1u; }
   }
 }
 

@@ -79,6 +79,14 @@ def test_act_dual_edge_rows():
     _check_act(np.ascontiguousarray(x[::-1]), transposed=True)
 
 
+def test_act_dual_edge_columns():
+    """The hand-built groups as 128x1 column groups (zero, -0, tiny, ties, huge)."""
+    e = _edge_rows(128)
+    block = np.concatenate([e, synth.normal_bf16((128 - e.shape[0], 128), 1.0, 1, 3, outliers=True)])
+    x = np.ascontiguousarray(np.concatenate([block.T, block[::-1].T], axis=0))   # [256, 128]
+    _check_act(x, transposed=True)
+
+
 @pytest.mark.parametrize("N,K", [(128, 128), (256, 512), (384, 1024)])
 def test_weight_random(N, K):
     torch, fp8bs = require_gpu()
@@ -106,6 +114,10 @@ def test_weight_edge_blocks():
     q_ref, s_ref = oracle.quantize_weight_128x128(bits)
     assert_bytes_equal(to_host(wq), q_ref, "codes")
     assert_scales_equal(to_host(sw), s_ref, "scales")
+    wq, sw, wq_t, sw_t = fp8bs.quantize_weight(to_dev_bf16(bits), transposed=True)
+    assert_bytes_equal(to_host(wq), q_ref, "codes (with transposed copy)")
+    assert_bytes_equal(to_host(wq_t), q_ref.T, "transposed codes")
+    assert_scales_equal(to_host(sw_t), s_ref.T, "transposed scales")
 
 
 def test_empty_inputs_are_no_ops():
