@@ -12,7 +12,11 @@ run and reported beside it:
   * ``roofline``: the GEMM against the FP8 dense tensor peak;
   * ``e2e``:      the step through the public API with host buffers (pinned
                   host -> device copies of X and W, device -> host copy of Y);
-  * ``cpu_baseline``: the CPU oracle on a bounded sample of the same step.
+  * ``cpu_baseline``: the CPU oracle on a bounded sample of the same step;
+  * ``workloads``: the other configurations, each kernel timed alone: the
+                  MoE grouped GEMMs (gate/up and down), dgrad, wgrad, the
+                  dual-layout (1x128 + 128x1) activation quantize and the
+                  weight quantize with its transposed copy.
 
 Multi-GPU: every rank runs its own replica on its own batch (data
 parallel, no collective on the data path); ``value`` sums all ranks' FLOPs
@@ -198,6 +202,127 @@ def run_reference(args):
 
 # ----------------------------------------------------------------- GPU arm
 
+def _time_ms(fn, stream, warmup: int, reps: int) -> float:
+    """Mean device time of fn() on `stream` (CUDA events around each call)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm_peak: float, warmup: int):
+    """The other configurations of the path, each kernel timed alone.
+
+    * MoE grouped fprop: 8192 tokens, top-8 of 32 experts (Zipf s=1.1),
+      per-expert rows padded to 128; gate/up [67712 x 4096 x 7168] and down
+      [67712 x 7168 x 2048], BF16 out.  Routing and token activations follow
+      the numpy recipe; the expert weights N(0,0.02) and the down-projection
+      input N(0,1) are drawn on the device by torch's seeded generator (same
+      distributions, BF16-rounded) so the 1.4 G weights take no host time.
+      TFLOP/s counts real (unpadded) rows.
+    * dgrad dX[4096,2048] = dY[4096,7168] W[7168,2048] (FP32 out, B = the
+      transposed weight copy); wgrad dW[2048,7168] = dY^T X over T = 16384
+      (both 128x1 along T, row-scaled B, FP32 out).
+    * quantize with the transposed 128x1 output, X[16384,7168]; weight
+      quantize W[7168,7168] with its transposed copy.
+    """
+    import torch
+    out = {}
+    reps = 10
+
+    def gemm_line(flop, ms, **extra):
+        tf = flop / (ms * 1e-3) / 1e12
+        return {"tflops": tf, "ms": ms, "frac_of_fp8_peak": tf / fp8_peak, "gflop": flop / 1e9, **extra}
+
+    def bw_line(nbytes, ms, **extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"gbs": gbs, "ms": ms, "frac_of_hbm": gbs / hbm_peak, "bytes": nbytes, **extra}
+
+    # ---- dgrad
+    dy_bits, w_bits = synth.dgrad(seed=rank)
+    dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    w = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    dyq, sdy = fp8bs.quantize_act(dy)
+    _, _, wq_t, sw_t = fp8bs.quantize_weight(w, transposed=True)
+    dx = torch.empty((4096, 2048), dtype=torch.float32, device=dev)
+    ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq, sdy, wq_t, sw_t, fp8bs.SCALE_BLOCK128x128, dx, fp8bs.OUT_F32,
+                                           4096, 2048, 7168, 0, stream), stream, warmup, reps)
+    out["dgrad"] = gemm_line(2.0 * 4096 * 2048 * 7168, ms, shape="M=4096 N=2048 K=7168, FP32 out")
+    del dy, w, dyq, sdy, wq_t, sw_t, dx
+
+    # ---- wgrad (+ the dual-layout quantize of its operands)
+    dy_bits, x_bits = synth.wgrad(seed=rank)
+    dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    _, _, dyq_t, sdy_t = fp8bs.quantize_act(dy, transposed=True)
+    xq, sx, xq_t, sx_t = fp8bs.quantize_act(x, transposed=True)
+    dw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
+    ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq_t, sdy_t, xq_t, sx_t, fp8bs.SCALE_ROW1x128, dw, fp8bs.OUT_F32,
+                                           2048, 7168, 16384, 0, stream), stream, warmup, reps)
+    out["wgrad"] = gemm_line(2.0 * 2048 * 7168 * 16384, ms, shape="M=2048 N=7168 K=T=16384, row-scaled B, FP32 out")
+    T_, K_ = x.shape
+    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act(x, T_, K_, K_, xq, sx, xq_t, sx_t, stream), stream, warmup, reps)
+    out["quantize_dual"] = bw_line(T_ * K_ * (2 + 1 + 1) + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
+                                   shape="X[16384,7168] -> 1x128 and 128x1")
+    del dy, x, dyq_t, sdy_t, xq, sx, xq_t, sx_t, dw
+
+    # ---- weight quantize with the transposed copy
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    wbig = (torch.randn((7168, 7168), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    wq, sw, wq_t2, sw_t2 = fp8bs.quantize_weight(wbig, transposed=True)
+    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_weight(wbig, 7168, 7168, 7168, wq, sw, wq_t2, sw_t2, stream),
+                  stream, warmup, reps)
+    out["quantize_weight"] = bw_line(7168 * 7168 * (2 + 1 + 1) + 2 * 56 * 56 * 4, ms,
+                                     shape="W[7168,7168] -> 128x128 blocks + transposed copy")
+    del wbig, wq, sw, wq_t2, sw_t2
+
+    # ---- MoE grouped fprop
+    E, H, I = 32, 7168, 2048
+    choice = synth.moe_routing(seed=rank)
+    offsets_np, src_np = synth.moe_layout(choice, E)
+    rows = int(offsets_np[-1])
+    real_rows = int((src_np >= 0).sum())
+    x_tok = torch.from_numpy(synth.normal_bf16((8192, H), 1.0, rank, synth.TID_X, outliers=True).view(np.int16))
+    x_tok = x_tok.view(torch.bfloat16).to(dev)
+    src = torch.from_numpy(src_np).to(dev)
+    x_rows = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
+    ok = src >= 0
+    x_rows[ok] = x_tok[src[ok]]
+    offsets = torch.from_numpy(offsets_np).to(dev)
+    w_gu = (torch.randn((E * 2 * I, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    w_dn = (torch.randn((E * H, I), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    d_in = torch.randn((rows, I), generator=g, device=dev).to(torch.bfloat16)
+    d_in[~ok] = 0
+    aq, sa = fp8bs.quantize_act(x_rows)
+    bq, sb = fp8bs.quantize_weight(w_gu)
+    y1 = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+    ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y1, fp8bs.OUT_BF16, 2 * I, H,
+                                                   stream), stream, warmup, reps)
+    out["moe_gate_up"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
+                                   shape=f"grouped 32 experts, [{rows} x {2 * I} x {H}], BF16 out")
+    del aq, sa, bq, sb, y1, x_rows, w_gu
+    aq, sa = fp8bs.quantize_act(d_in)
+    bq, sb = fp8bs.quantize_weight(w_dn)
+    y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y2, fp8bs.OUT_BF16, H, I,
+                                                   stream), stream, warmup, reps)
+    out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
+                                shape=f"grouped 32 experts, [{rows} x {H} x {I}], BF16 out")
+    del aq, sa, bq, sb, y2, d_in, w_dn
+    if fp8bs.fp8bs_get_device_status(stream) != 0:
+        raise RuntimeError("device status after the workload measurements")
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -205,6 +330,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="fp8bs", choices=["fp8bs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-kernel lines of the MoE, dgrad, wgrad and quantize variants")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -328,6 +455,9 @@ def main():
 
     peaks, peak_src = _peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    workloads = None
+    if not args.no_workloads:
+        workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup)
     gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
     value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
@@ -366,6 +496,8 @@ def main():
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if workloads is not None:
+        line["workloads"] = workloads
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x_bits, w_bits)
     if world > 1:
