@@ -27,6 +27,8 @@ design notes of the repository):
     before the rounding to E4M3;
   * the stored scale is s itself (float32), not 1/s;
   * a group whose absmax is 0 gets s = 0 and all-zero codes;
+  * power-of-two ("rounded") scales, §3.3.3 (1): the smallest 2^k with
+    absmax / 2^k <= 448;
   * the GEMM reference value of each 128-wide K block is its exact sum
     (computed in float64, where it is exact), scaled by s_a * s_b in
     float64 and summed over the blocks in float64.
@@ -36,12 +38,14 @@ no numeric output of a quantised tile or GEMM.
 """
 from .e4m3 import (E4M3_MAX, e4m3_decode, e4m3_encode, e4m3_all_finite_values)
 from .quantize import (quantize_groups, quantize_act_1x128, quantize_act_128x1,
-                       quantize_weight_128x128, bf16_bits_to_f32)
+                       quantize_weight_128x128, bf16_bits_to_f32, pow2_scale,
+                       dequantize_1x128, requant_1x128_to_128x1)
 from .gemm import gemm_block_scaled, grouped_gemm_block_scaled, bf16_round
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_all_finite_values",
     "quantize_groups", "quantize_act_1x128", "quantize_act_128x1",
-    "quantize_weight_128x128", "bf16_bits_to_f32",
+    "quantize_weight_128x128", "bf16_bits_to_f32", "pow2_scale",
+    "dequantize_1x128", "requant_1x128_to_128x1",
     "gemm_block_scaled", "grouped_gemm_block_scaled", "bf16_round",
 ]
