@@ -22,13 +22,15 @@ from .build import LIB_PATH, build as _build
 __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
+    "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string",
-    "quantize_act", "quantize_weight", "gemm", "grouped_gemm",
-    "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128",
+    "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1",
+    "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128", "SCALE_ABSMAX", "SCALE_POW2",
 ]
 
 OUT_F32, OUT_BF16 = 0, 1
 SCALE_BLOCK128x128, SCALE_ROW1x128 = 0, 1
+SCALE_ABSMAX, SCALE_POW2 = 0, 1
 
 STATUS_NAMES = {0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_SHAPE", 3: "FP8BS_ERR_ALIGNMENT",
                 4: "FP8BS_ERR_UNSUPPORTED_ARCH", 5: "FP8BS_ERR_CUDA", 6: "FP8BS_ERR_TIMEOUT",
@@ -48,6 +50,9 @@ _c_i64, _c_int, _c_vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 _SIGNATURES = {
     "fp8bs_quantize_act": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp],
     "fp8bs_quantize_weight": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp],
+    "fp8bs_quantize_act_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
+    "fp8bs_quantize_weight_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
+    "fp8bs_requant_1x128_to_128x1": [_c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_gemm": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
     "fp8bs_grouped_gemm": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                            _c_vp],
@@ -115,6 +120,24 @@ def fp8bs_quantize_weight(w, N, K, ldw, wq, sw, wq_t=None, sw_t=None, stream=Non
                                      _stream(stream)), "fp8bs_quantize_weight")
 
 
+def fp8bs_quantize_act_ex(x, M, K, ldx, xq, sx, xq_t=None, sx_t=None, scale_mode=SCALE_ABSMAX, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_quantize_act_ex(_ptr(x), M, K, ldx, _ptr(xq), _ptr(sx), _ptr(xq_t), _ptr(sx_t),
+                                     int(scale_mode), _stream(stream)), "fp8bs_quantize_act_ex")
+
+
+def fp8bs_quantize_weight_ex(w, N, K, ldw, wq, sw, wq_t=None, sw_t=None, scale_mode=SCALE_ABSMAX, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_quantize_weight_ex(_ptr(w), N, K, ldw, _ptr(wq), _ptr(sw), _ptr(wq_t), _ptr(sw_t),
+                                        int(scale_mode), _stream(stream)), "fp8bs_quantize_weight_ex")
+
+
+def fp8bs_requant_1x128_to_128x1(xq, sx, M, K, xq_t, sx_t, scale_mode=SCALE_POW2, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_requant_1x128_to_128x1(_ptr(xq), _ptr(sx), M, K, _ptr(xq_t), _ptr(sx_t), int(scale_mode),
+                                            _stream(stream)), "fp8bs_requant_1x128_to_128x1")
+
+
 def fp8bs_gemm(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate=0, stream=None):
     lib = load_library()
     _check(lib.fp8bs_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), sb_kind, _ptr(d), d_dtype, M, N, K,
@@ -141,11 +164,12 @@ def fp8bs_status_string(status: int) -> str:
 
 # ------------------------------------------------------ allocating conveniences
 
-def quantize_act(x, transposed: bool = False, stream=None):
+def quantize_act(x, transposed: bool = False, pow2: bool = False, stream=None):
     """x: [M, K] bfloat16 CUDA tensor (row-major, K % 128 == 0).
 
     Returns (xq [M,K] uint8, sx [K/128, M] float32) and, with ``transposed``,
-    also (xq_t [K,M] uint8, sx_t [M/128, K] float32).
+    also (xq_t [K,M] uint8, sx_t [M/128, K] float32).  ``pow2`` selects
+    power-of-two scales (SCALE_POW2).
     """
     import torch
     M, K = x.shape
@@ -155,11 +179,11 @@ def quantize_act(x, transposed: bool = False, stream=None):
     if transposed:
         xq_t = torch.empty((K, M), dtype=torch.uint8, device=x.device)
         sx_t = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
-    fp8bs_quantize_act(x, M, K, x.stride(0), xq, sx, xq_t, sx_t, stream)
+    fp8bs_quantize_act_ex(x, M, K, x.stride(0), xq, sx, xq_t, sx_t, SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
     return (xq, sx, xq_t, sx_t) if transposed else (xq, sx)
 
 
-def quantize_weight(w, transposed: bool = False, stream=None):
+def quantize_weight(w, transposed: bool = False, pow2: bool = False, stream=None):
     """w: [N, K] bfloat16 CUDA tensor.  Returns (wq, sw[, wq_t, sw_t])."""
     import torch
     N, K = w.shape
@@ -169,8 +193,19 @@ def quantize_weight(w, transposed: bool = False, stream=None):
     if transposed:
         wq_t = torch.empty((K, N), dtype=torch.uint8, device=w.device)
         sw_t = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
-    fp8bs_quantize_weight(w, N, K, w.stride(0), wq, sw, wq_t, sw_t, stream)
+    fp8bs_quantize_weight_ex(w, N, K, w.stride(0), wq, sw, wq_t, sw_t, SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
     return (wq, sw, wq_t, sw_t) if transposed else (wq, sw)
+
+
+def requant_1x128_to_128x1(xq, sx, pow2: bool = True, stream=None):
+    """Re-tile 1x128-quantised activations (xq [M,K] uint8, sx [K/128, M]) into
+    128x1 groups: returns (xq_t [K,M] uint8, sx_t [M/128, K] float32)."""
+    import torch
+    M, K = xq.shape
+    xq_t = torch.empty((K, M), dtype=torch.uint8, device=xq.device)
+    sx_t = torch.empty((M // 128, K), dtype=torch.float32, device=xq.device)
+    fp8bs_requant_1x128_to_128x1(xq, sx, M, K, xq_t, sx_t, SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
+    return xq_t, sx_t
 
 
 def gemm(a, sa, b, sb, sb_kind: int = SCALE_BLOCK128x128, out_dtype=None, out=None, accumulate: bool = False,

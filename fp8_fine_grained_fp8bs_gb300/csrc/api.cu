@@ -49,9 +49,10 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CU
 
 extern "C" {
 
-int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx, uint8_t* xq_t,
-                       float* sx_t, void* stream) {
+int fp8bs_quantize_act_ex(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx, uint8_t* xq_t,
+                          float* sx_t, int scale_mode, void* stream) {
   if (M < 0 || K < 0 || ldx < K) return FP8BS_ERR_INVALID_ARG;
+  if (scale_mode != FP8BS_SCALE_ABSMAX && scale_mode != FP8BS_SCALE_POW2) return FP8BS_ERR_INVALID_ARG;
   if ((xq_t == nullptr) != (sx_t == nullptr)) return FP8BS_ERR_INVALID_ARG;
   if (M > 0 && K > 0 && (x == nullptr || xq == nullptr || sx == nullptr)) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0) return FP8BS_ERR_SHAPE;
@@ -66,14 +67,21 @@ int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t
   const auto* xb = static_cast<const uint16_t*>(x);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint64_t tmo = g_timeout_ns.load();
+  const bool pow2 = scale_mode == FP8BS_SCALE_POW2;
   if (xq_t != nullptr)
-    return from_cuda(fp8bs::launch_quantize_act_dual(xb, M, K, ldx, xq, sx, xq_t, sx_t, sms, tmo, s));
-  return from_cuda(fp8bs::launch_quantize_act_1x128(xb, M, K, ldx, xq, sx, sms, tmo, s));
+    return from_cuda(fp8bs::launch_quantize_act_dual(xb, M, K, ldx, xq, sx, xq_t, sx_t, pow2, sms, tmo, s));
+  return from_cuda(fp8bs::launch_quantize_act_1x128(xb, M, K, ldx, xq, sx, pow2, sms, tmo, s));
 }
 
-int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw, uint8_t* wq_t,
-                          float* sw_t, void* stream) {
+int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx, uint8_t* xq_t,
+                       float* sx_t, void* stream) {
+  return fp8bs_quantize_act_ex(x, M, K, ldx, xq, sx, xq_t, sx_t, FP8BS_SCALE_ABSMAX, stream);
+}
+
+int fp8bs_quantize_weight_ex(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw,
+                             uint8_t* wq_t, float* sw_t, int scale_mode, void* stream) {
   if (N < 0 || K < 0 || ldw < K) return FP8BS_ERR_INVALID_ARG;
+  if (scale_mode != FP8BS_SCALE_ABSMAX && scale_mode != FP8BS_SCALE_POW2) return FP8BS_ERR_INVALID_ARG;
   if ((wq_t == nullptr) != (sw_t == nullptr)) return FP8BS_ERR_INVALID_ARG;
   if (N > 0 && K > 0 && (w == nullptr || wq == nullptr || sw == nullptr)) return FP8BS_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
@@ -83,8 +91,30 @@ int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint
   int sms = 0;
   const int st = current_device(&sms);
   if (st != FP8BS_OK) return st;
-  return from_cuda(fp8bs::launch_quantize_weight(static_cast<const uint16_t*>(w), N, K, ldw, wq, sw, wq_t, sw_t, sms,
-                                                 g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
+  return from_cuda(fp8bs::launch_quantize_weight(static_cast<const uint16_t*>(w), N, K, ldw, wq, sw, wq_t, sw_t,
+                                                 scale_mode == FP8BS_SCALE_POW2, sms, g_timeout_ns.load(),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw, uint8_t* wq_t,
+                          float* sw_t, void* stream) {
+  return fp8bs_quantize_weight_ex(w, N, K, ldw, wq, sw, wq_t, sw_t, FP8BS_SCALE_ABSMAX, stream);
+}
+
+int fp8bs_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,
+                                 float* sx_t, int scale_mode, void* stream) {
+  if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (scale_mode != FP8BS_SCALE_ABSMAX && scale_mode != FP8BS_SCALE_POW2) return FP8BS_ERR_INVALID_ARG;
+  if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (xq == nullptr || sx == nullptr || xq_t == nullptr || sx_t == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(sx) || !aligned16(xq_t) || !aligned16(sx_t)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_requant_1x128_to_128x1(xq, sx, M, K, xq_t, sx_t, scale_mode == FP8BS_SCALE_POW2, sms,
+                                                        static_cast<cudaStream_t>(stream)));
 }
 
 static int run_gemm(const fp8bs::GemmArgs& args, void* stream) {

@@ -11,14 +11,19 @@ namespace fp8bs {
 // Every quantiser streams 128x128 BF16 tiles through shared memory with
 // TMA; its waits are bounded by timeout_ns and a wait that expires records
 // FP8BS_ERR_TIMEOUT in the status word that quant_take_status reads.
+// pow2: power-of-two scales instead of fl32(absmax / 448).
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                      float* sx, int sm_count, uint64_t timeout_ns, cudaStream_t stream);
+                                      float* sx, bool pow2, int sm_count, uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                     float* sx, uint8_t* xq_t, float* sx_t, int sm_count, uint64_t timeout_ns,
-                                     cudaStream_t stream);
+                                     float* sx, uint8_t* xq_t, float* sx_t, bool pow2, int sm_count,
+                                     uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
-                                   float* sw, uint8_t* wq_t, float* sw_t, int sm_count, uint64_t timeout_ns,
-                                   cudaStream_t stream);
+                                   float* sw, uint8_t* wq_t, float* sw_t, bool pow2, int sm_count,
+                                   uint64_t timeout_ns, cudaStream_t stream);
+// FP8 -> FP8 re-tiling 1x128 -> 128x1 (dequantise, transpose, requantise);
+// plain loads, no waits.
+cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,
+                                          float* sx_t, bool pow2, int sm_count, cudaStream_t stream);
 // Reads and clears the quantisers' device status word (synchronous copy on
 // the current device).
 cudaError_t quant_take_status(int* status);

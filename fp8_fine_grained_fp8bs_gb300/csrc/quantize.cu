@@ -8,6 +8,7 @@
 // The per-element quotient is decided from a two-sided bracket of x * (1/s)
 // (quant8m below) with IEEE divisions only where the bracket is
 // inconclusive, so every byte is read once and written once.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -89,6 +90,54 @@ __device__ __forceinline__ Divisor table_divisor(const DivTable& t, uint32_t a16
   d.r_up = __uint_as_float(t.rup[f] - (static_cast<uint32_t>(sh) << 23));
   d.fast = true;
   return d;
+}
+
+// Power-of-two ("rounded") scale, §3.3.3 "low-precision activations" (1):
+// s = 2^k, the smallest power of two with absmax / s <= 448, k >= -149 (the
+// smallest positive float32).  x / s is then exact, so the bracket is a
+// single exact product (r_lo = r_up = 2^-k) whenever 2^-k is a normal
+// float32; scales below 2^-127 take the exact division path.
+__device__ __forceinline__ Divisor pow2_from_exp(int k) {
+  k = max(k, -149);
+  Divisor d;
+  d.s = k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23) : __uint_as_float(1u << (k + 149));
+  d.fast = k >= -127 && k <= 126;
+  const float r = d.fast ? __uint_as_float(static_cast<uint32_t>(127 - k) << 23) : 1.0f;
+  d.r_lo = r;
+  d.r_up = r;
+  return d;
+}
+
+// absmax a = m * 2^e with m in [1, 2): a / 448 = (m / 1.75) * 2^(e - 8) and
+// m / 1.75 lies in (0.5, 1.143), so k = e - 8, plus 1 when m > 1.75.
+__device__ __forceinline__ Divisor pow2_divisor_f32(float a) {
+  if (!(a > 0.0f)) {
+    Divisor d;
+    d.s = 0.0f;
+    d.r_lo = d.r_up = 1.0f;
+    d.fast = false;
+    return d;
+  }
+  uint32_t b = __float_as_uint(a);
+  int bias = 0;
+  if ((b >> 23) == 0) {  // subnormal: scale up by 2^64 (exact) and take it back from the exponent
+    b = __float_as_uint(a * 18446744073709551616.0f);
+    bias = 64;
+  }
+  const int e = static_cast<int>(b >> 23) - 127 - bias;
+  return pow2_from_exp(e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0));
+}
+
+// The same from BF16 absmax bits (1.75 = 1 + 96/128 in BF16's 7-bit fraction).
+__device__ __forceinline__ Divisor pow2_divisor_bits(uint32_t a16) {
+  const uint32_t e = a16 >> 7;
+  if (e == 0) return pow2_divisor_f32(__uint_as_float(a16 << 16));
+  return pow2_from_exp(static_cast<int>(e) - 127 - 8 + ((a16 & 0x7Fu) > 96u ? 1 : 0));
+}
+
+// Divisor of a group from its BF16 absmax bits, in the requested scale mode.
+__device__ __forceinline__ Divisor group_divisor(const DivTable& t, uint32_t a16, bool pow2) {
+  return pow2 ? pow2_divisor_bits(a16) : table_divisor(t, a16);
 }
 
 // Largest |x| of BF16 values: for non-negative floats the integer order of
@@ -223,6 +272,7 @@ struct TileParams {
   uint8_t* q_t;     // dual: [K][rows] codes of the 128x1 groups; weight: transposed codes; or null
   float* s_t;       // dual: [nrb][K]; weight: [nkb][nrb]; or null
   uint64_t timeout_ns;
+  int pow2;         // power-of-two scales instead of absmax / 448
 };
 
 struct QShared {
@@ -418,14 +468,14 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         uint32_t a = S.red[par][0];
 #pragma unroll
         for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
-        d = table_divisor(S.tab, a);
+        d = group_divisor(S.tab, a, p.pow2 != 0);
         if (t == 0) p.s[rb * p.nkb + kb] = d.s;
       } else {
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
           break;
         }
-        d = table_divisor(S.tab, m & 0xFFFFu);
+        d = group_divisor(S.tab, m & 0xFFFFu, p.pow2 != 0);
         if (h == 0 && row < p.rows) p.s[static_cast<int64_t>(kb) * p.rows + row] = d.s;
       }
       if (row < p.rows) quant_row64(w, d, h, rowp, rsw, p.q + row * K + static_cast<int64_t>(kb) * kGroup + 64 * h);
@@ -462,7 +512,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       uint32_t a = S.red[par][0];
 #pragma unroll
       for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
-      const Divisor d = table_divisor(S.tab, a);
+      const Divisor d = group_divisor(S.tab, a, p.pow2 != 0);
       if (t == 0) {
         p.s[rb * p.nkb + kb] = d.s;
         p.s_t[static_cast<int64_t>(kb) * p.nrb + rb] = d.s;
@@ -507,7 +557,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
-        const Divisor d = table_divisor(S.tab, a16);
+        const Divisor d = group_divisor(S.tab, a16, p.pow2 != 0);
         uint32_t bm = 0;
         const uint2 q = quant8m(v[j], d, bm);
         rowbad |= bm << (4 * j);
@@ -548,15 +598,15 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t]);
         S.colmax[t] = m;
         float* st = p.s_t + rb * K + static_cast<int64_t>(kb) * kGroup + 2 * t;
-        st[0] = table_divisor(S.tab, m & 0xFFFFu).s;
-        st[1] = table_divisor(S.tab, m >> 16).s;
+        st[0] = group_divisor(S.tab, m & 0xFFFFu, p.pow2 != 0).s;
+        st[1] = group_divisor(S.tab, m >> 16, p.pow2 != 0).s;
       }
       compute_bar();
       uint32_t colbad = 0;  // bit 4i+m: rows 2m, 2m+1 of column i need the exact path
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t m = S.colmax[4 * c + (i >> 1)];
-        const Divisor d = table_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu));
+        const Divisor d = group_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
         uint32_t bm = 0;
         const uint2 q = quant8m(vt[i], d, bm);
         colbad |= bm << (4 * i);
@@ -566,7 +616,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         const int b = __ffs(rowbad) - 1;
         rowbad &= rowbad - 1u;
         const int j = b >> 2, k = b & 3;
-        const float sj = table_divisor(S.tab, S.rowabs[8 * g + j]).s;
+        const float sj = group_divisor(S.tab, S.rowabs[8 * g + j], p.pow2 != 0).s;
         const uint32_t e = quant2_exact(*reinterpret_cast<const uint32_t*>(src + j * kTileRowBytes + 4 * k), sj);
         *reinterpret_cast<uint16_t*>(p.q + (r0 + j) * K + c0 + 2 * k) = static_cast<uint16_t>(e);
       }
@@ -575,7 +625,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         colbad &= colbad - 1u;
         const int i = b >> 2, m = b & 3;
         const uint32_t cm = S.colmax[4 * c + (i >> 1)];
-        const float si = table_divisor(S.tab, (i & 1) ? (cm >> 16) : (cm & 0xFFFFu)).s;
+        const float si = group_divisor(S.tab, (i & 1) ? (cm >> 16) : (cm & 0xFFFFu), p.pow2 != 0).s;
         const uint16_t* col = reinterpret_cast<const uint16_t*>(src + 2 * m * kTileRowBytes) + i;
         const uint32_t wd = static_cast<uint32_t>(col[0]) | (static_cast<uint32_t>(col[kTileRowBytes / 2]) << 16);
         *reinterpret_cast<uint16_t*>(p.q_t + (c0 + i) * p.rows + r0 + 2 * m) =
@@ -629,27 +679,183 @@ cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Re-tiling from FP8 (§3.5.2 "support for transposed GEMM operations": the
+// backward pass reads the 1x128-quantised activations, dequantises them,
+// transposes and requantises them in 128x1 groups; with power-of-two scales,
+// §3.3.3 (1), this adds no quantisation error).  One 128x128 tile per step:
+// thread t holds rows 8*(t/16) .. +7 of the 8-column chunk t%16 of the tile
+// (eight 8-byte code rows, read coalesced straight from global memory, the
+// next tile's already in flight), dequantises them with their row scales,
+// reduces the column maxima (shuffle, then shared memory across the eight
+// warps), and quantises each column's 8 values into 8 consecutive bytes of
+// X^T.
+constexpr int kRqThreads = 256;
+
+struct RequantParams {
+  const uint8_t* xq;  // [M][K] codes of the 1x128 groups
+  const float* sx;    // [K/128][M] their scales, kb-major
+  int64_t M, K;
+  int nkb;
+  int64_t ntiles;
+  uint8_t* xq_t;      // [K][M] codes of the 128x1 groups
+  float* sx_t;        // [M/128][K]
+  int pow2;
+};
+
+// Eight float32 values -> eight codes with one divisor (bracketed products,
+// as quant_pair); bit j of `bad` flags pair j for the exact path.
+__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d, uint32_t& bad) {
+  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
+  uint32_t c[4];
+  bad = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
+    const float2 l = __fmul2_rz(a, rlo);
+    const float2 u = __fmul2_rz(a, rup);
+    c[j] = e4m3x2(l.x, l.y);
+    bad |= ((c[j] != e4m3x2(u.x, u.y)) || !d.fast ? 1u : 0u) << j;
+  }
+  if (d.s == 0.0f) return make_uint2(0u, 0u);
+  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+}
+
+__device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
+  return pow2 ? pow2_divisor_f32(a) : make_divisor(a);
+}
+
+__global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantParams p) {
+  __shared__ uint32_t colred[kRqThreads / 32][kGroup];  // per-warp column maxima (|v| bits)
+  __shared__ float colmax[kGroup];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int g = t >> 4, c = t & 15;
+  uint2 nq[8];
+  auto load = [&](int64_t tile, uint2 (&q)[8]) {
+    if (tile >= p.ntiles) return;
+    const int64_t rb = tile / p.nkb;
+    const int kb = static_cast<int>(tile - rb * p.nkb);
+    const uint8_t* src = p.xq + (rb * kGroup + 8 * g) * p.K + static_cast<int64_t>(kb) * kGroup + 8 * c;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = __ldg(reinterpret_cast<const uint2*>(src + j * p.K));
+  };
+  load(blockIdx.x, nq);
+  for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+    uint2 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = nq[j];
+    load(tile + gridDim.x, nq);
+    const int64_t rb = tile / p.nkb;
+    const int kb = static_cast<int>(tile - rb * p.nkb);
+    const int64_t r0 = rb * kGroup + 8 * g;
+    const float4 s_lo = __ldg(reinterpret_cast<const float4*>(p.sx + static_cast<int64_t>(kb) * p.M + r0));
+    const float4 s_hi = __ldg(reinterpret_cast<const float4*>(p.sx + static_cast<int64_t>(kb) * p.M + r0 + 4));
+    const float sr[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+    // dequantise: v[i][j] = column i, row j of the thread's 8x8 sub-block
+    float v[8][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w2[2] = {q[j].x, q[j].y};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        v[2 * h][j] = __fmul_rn(f.x, sr[j]);
+        v[2 * h + 1][j] = __fmul_rn(f.y, sr[j]);
+      }
+    }
+    // column maxima of |v| (non-negative floats order like their bits)
+    uint32_t m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t a = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a = max(a, __float_as_uint(v[i][j]) & 0x7FFFFFFFu);
+      m[i] = max(a, __shfl_xor_sync(0xffffffffu, a, 16));  // the other row group of this warp
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) colred[warp][8 * c + i] = m[i];
+    }
+    __syncthreads();
+    if (t < kGroup) {
+      uint32_t a = colred[0][t];
+#pragma unroll
+      for (int w = 1; w < kRqThreads / 32; ++w) a = max(a, colred[w][t]);
+      const float amax = __uint_as_float(a);
+      colmax[t] = amax;
+      p.sx_t[rb * p.K + static_cast<int64_t>(kb) * kGroup + t] = divisor_f32(amax, p.pow2 != 0).s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const Divisor d = divisor_f32(colmax[8 * c + i], p.pow2 != 0);
+      uint32_t bad;
+      uint2 code = quant8f(v[i], d, bad);
+      if (bad != 0u) {  // pairs whose bracket straddles an E4M3 rounding boundary: IEEE divisions
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (!(bad & (1u << k))) continue;
+          const uint32_t e =
+              d.s == 0.0f ? 0u : e4m3x2(__fdiv_rn(v[i][2 * k], d.s), __fdiv_rn(v[i][2 * k + 1], d.s));
+          uint32_t& word = k < 2 ? code.x : code.y;
+          const int sh = 16 * (k & 1);
+          word = (word & ~(0xFFFFu << sh)) | (e << sh);
+        }
+      }
+      *reinterpret_cast<uint2*>(p.xq_t + (static_cast<int64_t>(kb) * kGroup + 8 * c + i) * p.M + r0) = code;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                      float* sx, int sm_count, uint64_t timeout_ns, cudaStream_t stream) {
-  const TileParams p{M, (M + kGroup - 1) / kGroup, static_cast<int>(K / kGroup), xq, sx, nullptr, nullptr, timeout_ns};
+                                      float* sx, bool pow2, int sm_count, uint64_t timeout_ns, cudaStream_t stream) {
+  const TileParams p{M,       (M + kGroup - 1) / kGroup, static_cast<int>(K / kGroup), xq, sx, nullptr, nullptr,
+                     timeout_ns, pow2 ? 1 : 0};
   return launch_tiles<kModeAct>(x, ldx, p, sm_count, stream);
 }
 
 cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
-                                     float* sx, uint8_t* xq_t, float* sx_t, int sm_count, uint64_t timeout_ns,
-                                     cudaStream_t stream) {
-  const TileParams p{M, M / kGroup, static_cast<int>(K / kGroup), xq, sx, xq_t, sx_t, timeout_ns};
+                                     float* sx, uint8_t* xq_t, float* sx_t, bool pow2, int sm_count,
+                                     uint64_t timeout_ns, cudaStream_t stream) {
+  const TileParams p{M, M / kGroup, static_cast<int>(K / kGroup), xq, sx, xq_t, sx_t, timeout_ns, pow2 ? 1 : 0};
   return launch_tiles<kModeDual>(x, ldx, p, sm_count, stream);
 }
 
 cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
-                                   float* sw, uint8_t* wq_t, float* sw_t, int sm_count, uint64_t timeout_ns,
-                                   cudaStream_t stream) {
-  const TileParams p{N, N / kGroup, static_cast<int>(K / kGroup), wq, sw, wq_t, sw_t, timeout_ns};
+                                   float* sw, uint8_t* wq_t, float* sw_t, bool pow2, int sm_count,
+                                   uint64_t timeout_ns, cudaStream_t stream) {
+  const TileParams p{N, N / kGroup, static_cast<int>(K / kGroup), wq, sw, wq_t, sw_t, timeout_ns, pow2 ? 1 : 0};
   if (wq_t != nullptr) return launch_tiles<kModeWeightT>(w, ldw, p, sm_count, stream);
   return launch_tiles<kModeWeight>(w, ldw, p, sm_count, stream);
+}
+
+cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,
+                                          float* sx_t, bool pow2, int sm_count, cudaStream_t stream) {
+  RequantParams p;
+  p.xq = xq;
+  p.sx = sx;
+  p.M = M;
+  p.K = K;
+  p.nkb = static_cast<int>(K / kGroup);
+  p.ntiles = (M / kGroup) * p.nkb;
+  p.xq_t = xq_t;
+  p.sx_t = sx_t;
+  p.pow2 = pow2 ? 1 : 0;
+  if (p.ntiles <= 0) return cudaSuccess;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, requant_kernel, kRqThreads, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+  requant_kernel<<<static_cast<int>(p.ntiles < slots ? p.ntiles : slots), kRqThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t quant_take_status(int* status) {

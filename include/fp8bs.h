@@ -69,6 +69,16 @@ typedef enum {
   FP8BS_SCALE_ROW1x128 = 1
 } fp8bs_b_scale_kind;
 
+typedef enum {
+  /* s = fl32(absmax / 448), the Figure 7 explainer's s = absmax / F_max. */
+  FP8BS_SCALE_ABSMAX = 0,
+  /* Power-of-two ("rounded") scale, §3.3.3 "low-precision activations" (1)
+   * and "low-precision communication": s = 2^k, the smallest power of two
+   * with absmax / s <= 448 (k >= -149).  Used for activations that are later
+   * re-tiled from 1x128 to 128x1, where it makes the re-tiling lossless. */
+  FP8BS_SCALE_POW2 = 1
+} fp8bs_scale_mode;
+
 /*
  * Activation quantisation, 1x128 tiles (§3.3.2 "fine-grained quantization"
  * (1) and "online quantization"), optionally also 128x1 tiles of the same
@@ -92,6 +102,14 @@ int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx,
                        uint8_t* xq, float* sx, uint8_t* xq_t, float* sx_t,
                        void* stream);
 
+/* fp8bs_quantize_act with a choice of scale (fp8bs_scale_mode): with
+ * FP8BS_SCALE_POW2 every group's scale is a power of two and each code is
+ * E4M3_rne_satfinite(x / s) (the quotient is exact).  Same arguments, rules
+ * and errors otherwise; an unknown scale_mode is FP8BS_ERR_INVALID_ARG. */
+int fp8bs_quantize_act_ex(const void* x, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t* xq, float* sx, uint8_t* xq_t, float* sx_t,
+                          int scale_mode, void* stream);
+
 /*
  * Weight quantisation, 128x128 blocks (§3.3.2 "fine-grained quantization"
  * (2); weights are quantised online too, "online quantization").
@@ -107,6 +125,30 @@ int fp8bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx,
 int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw,
                           uint8_t* wq, float* sw, uint8_t* wq_t, float* sw_t,
                           void* stream);
+
+/* fp8bs_quantize_weight with a choice of scale (fp8bs_scale_mode). */
+int fp8bs_quantize_weight_ex(const void* w, int64_t N, int64_t K, int64_t ldw,
+                             uint8_t* wq, float* sw, uint8_t* wq_t, float* sw_t,
+                             int scale_mode, void* stream);
+
+/*
+ * Backward re-tiling from FP8 (§3.5.2 "support for transposed GEMM
+ * operations": read the 1x128-quantised activations, dequantise, transpose,
+ * requantise in 128x1 tiles; §3.3.3 "low-precision activations" (1): with
+ * power-of-two scales this adds no quantisation error):
+ *
+ *   v[m][k]       = fl32(dec(xq[m][k]) * sx[kb*M + m])        (kb = k / 128)
+ *   group (k, tb) = v[128*tb .. 128*tb+127][k]
+ *   sx_t[tb*K + k] = scale of the group (scale_mode), xq_t[k][m] = its codes.
+ *
+ *   xq    [M][K] E4M3, 1x128 groups.  sx [K/128][M] float32, kb-major.   (in)
+ *   xq_t  [K][M] E4M3, 128x1 groups.  sx_t [M/128][K] float32.           (out)
+ * The outputs have the layout of fp8bs_quantize_act's xq_t / sx_t, so they
+ * feed the Wgrad GEMM (FP8BS_SCALE_ROW1x128) directly.
+ * Rules: M % 128 == 0, K % 128 == 0; all pointers 16-byte aligned.
+ */
+int fp8bs_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K,
+                                 uint8_t* xq_t, float* sx_t, int scale_mode, void* stream);
 
 /*
  * Block-scaled FP8 GEMM, D = A * B^T with per-128-K-block dequantisation

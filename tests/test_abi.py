@@ -69,6 +69,21 @@ def test_quantize_weight_argument_errors(lib):
     assert lib.fp8bs_quantize_weight(FAKE, 128, 128, 128, FAKE + 8, FAKE, None, None, None) == 3
 
 
+def test_scale_mode_and_requant_argument_errors(lib):
+    qa, qw, rq = lib.fp8bs_quantize_act_ex, lib.fp8bs_quantize_weight_ex, lib.fp8bs_requant_1x128_to_128x1
+    assert qa(FAKE, 128, 128, 128, FAKE, FAKE, None, None, 2, None) == 1          # unknown scale mode
+    assert qa(FAKE, 128, 100, 128, FAKE, FAKE, None, None, 1, None) == 2
+    assert qw(FAKE, 128, 128, 128, FAKE, FAKE, None, None, -1, None) == 1
+    assert qw(FAKE, 100, 128, 128, FAKE, FAKE, None, None, 1, None) == 2
+    assert rq(FAKE, FAKE, 100, 128, FAKE, FAKE, 1, None) == 2                     # M % 128
+    assert rq(FAKE, FAKE, 128, 100, FAKE, FAKE, 1, None) == 2                     # K % 128
+    assert rq(FAKE, FAKE, 128, 128, FAKE, FAKE, 3, None) == 1                     # scale mode
+    assert rq(FAKE, None, 128, 128, FAKE, FAKE, 1, None) == 1
+    assert rq(FAKE, FAKE, 128, 128, FAKE + 8, FAKE, 1, None) == 3
+    assert rq(FAKE, FAKE, -128, 128, FAKE, FAKE, 1, None) == 1
+    assert rq(None, None, 0, 128, None, None, 1, None) == 0                       # empty: no-op
+
+
 def test_gemm_argument_errors(lib):
     g = lib.fp8bs_gemm
     assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 100, 0, None) == 2   # K % 128
