@@ -15,8 +15,9 @@ run and reported beside it:
   * ``cpu_baseline``: the CPU oracle on a bounded sample of the same step;
   * ``workloads``: the other configurations, each kernel timed alone: the
                   MoE grouped GEMMs (gate/up and down), dgrad, wgrad, the
-                  dual-layout (1x128 + 128x1) activation quantize and the
-                  weight quantize with its transposed copy.
+                  dual-layout (1x128 + 128x1) activation quantize, the
+                  weight quantize with its transposed copy, the power-of-two
+                  scale quantize and the FP8 1x128 -> 128x1 re-tiling.
 
 Multi-GPU: every rank runs its own replica on its own batch (data
 parallel, no collective on the data path); ``value`` sums all ranks' FLOPs
@@ -231,7 +232,8 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
       transposed weight copy); wgrad dW[2048,7168] = dY^T X over T = 16384
       (both 128x1 along T, row-scaled B, FP32 out).
     * quantize with the transposed 128x1 output, X[16384,7168]; weight
-      quantize W[7168,7168] with its transposed copy.
+      quantize W[7168,7168] with its transposed copy; power-of-two scale
+      quantize and the FP8 re-tiling 1x128 -> 128x1 of the same X.
     """
     import torch
     out = {}
@@ -271,6 +273,16 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
     ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act(x, T_, K_, K_, xq, sx, xq_t, sx_t, stream), stream, warmup, reps)
     out["quantize_dual"] = bw_line(T_ * K_ * (2 + 1 + 1) + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
                                    shape="X[16384,7168] -> 1x128 and 128x1")
+    # power-of-two scales (§3.3.3 (1)) and the FP8 re-tiling 1x128 -> 128x1 (§3.5.2) of the same X
+    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act_ex(x, T_, K_, K_, xq, sx, None, None, fp8bs.SCALE_POW2, stream),
+                  stream, warmup, reps)
+    out["quantize_pow2"] = bw_line(T_ * K_ * (2 + 1) + T_ * (K_ // 128) * 4, ms,
+                                   shape="X[16384,7168] -> 1x128, power-of-two scales")
+    ms = _time_ms(lambda: fp8bs.fp8bs_requant_1x128_to_128x1(xq, sx, T_, K_, xq_t, sx_t, fp8bs.SCALE_POW2, stream),
+                  stream, warmup, reps)
+    out["requant_1x128_to_128x1"] = bw_line(T_ * K_ * 2 + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
+                                            shape="X[16384,7168] FP8 1x128 -> 128x1 (dequantise, transpose, "
+                                                  "requantise), power-of-two scales")
     del dy, x, dyq_t, sdy_t, xq, sx, xq_t, sx_t, dw
 
     # ---- weight quantize with the transposed copy

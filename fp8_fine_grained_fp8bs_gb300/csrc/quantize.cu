@@ -5,9 +5,10 @@
 // s = absmax / 448 and code = round(x / s).  Exactly as the C ABI states:
 // s = fl32(absmax / 448) and code = E4M3_rne_satfinite(fl32(x / s)), both
 // quotients IEEE round-to-nearest; a group with s == 0 gets all-zero codes.
-// The per-element quotient is decided from a two-sided bracket of x * (1/s)
-// (quant8m below) with IEEE divisions only where the bracket is
-// inconclusive, so every byte is read once and written once.
+// Each quotient is the correctly rounded x / s, obtained from the
+// reciprocal by Markstein's fused multiply-add correction (quant_pair
+// below), so every byte is read once and written once and no element needs
+// a division.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -23,88 +24,79 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Per-group divisor s with two reciprocals bracketing 1/s:
-//   r_lo = RD(1/s) <= 1/s,   r_up = RU(1/s) + 2 ulps,
-// where r_up is far enough above 1/s that a product truncated toward zero
-// still bounds the quotient: |RZ(x * r_up)| >= |x| / s.  (Truncation loses
-// less than 2^-23 of the product, the two extra ulps add at least 2^-23.)
+// Per-group divisor: s and y = RN(1/s).  Quotients use Markstein's
+// correctly rounded division by a fused multiply-add correction (P.
+// Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34(1), 1990):
+//   q0 = RN(x * y),  r = x - s * q0 (exact by one FMA),  q1 = RN(q0 + r * y),
+// which gives q1 = RN(x / s) when y = RN(1/s) and r does not underflow.  For
+// every quotient that can give a non-zero E4M3 code (|x / s| >= 2^-10) r is
+// exact once s >= 2^-93, and smaller quotients encode to a signed zero
+// either way; groups with s < 2^-93 (and s == 0) take IEEE divisions.  An
+// input of -0 yields q1 = +0, so the sign of x is ORed back into its code
+// (a no-op for every other input, whose code already has x's sign).
 struct Divisor {
   float s;
-  float r_lo, r_up;
-  bool fast;  // s is a normal float32; s == 0 and subnormal s take the exact path
+  float y;    // RN(1/s)
+  bool fast;  // s >= 2^-93: Markstein path; otherwise IEEE divisions
 };
 
-// RU(1/s) + 2 ulps from r_lo = RD(1/s): RU(1/s) is r_lo itself when 1/s is
-// exact (r_lo * s == 1, tested exactly by one fused multiply-add), else the
-// next float up.
-__device__ __forceinline__ float recip_up(float r_lo, float s) {
-  const uint32_t b = __float_as_uint(r_lo) + ((fmaf(r_lo, s, -1.0f) == 0.0f) ? 0u : 1u);
-  return __uint_as_float(b + 2u);
-}
+constexpr float kMinFastScale = 1.0097419586828951e-28f;  // 2^-93
 
 __device__ __forceinline__ Divisor make_divisor(float absmax) {
   Divisor d;
   d.s = __fdiv_rn(absmax, kE4M3Max);  // s = fl32(absmax / 448)
-  d.fast = d.s >= 1.17549435e-38f;    // FLT_MIN: 1/s is then a finite normal float
-  const float s = d.fast ? d.s : 1.0f;
-  d.r_lo = __frcp_rd(s);              // r_lo <= 1/s
-  d.r_up = recip_up(d.r_lo, s);
+  d.fast = d.s >= kMinFastScale;      // false for s == 0
+  d.y = __frcp_rn(d.fast ? d.s : 1.0f);
   return d;
 }
 
 // Table-driven divisor.  For a normal BF16 absmax a = (1 + f/128) * 2^e the
 // scale is s = fl32(a / 448) = fl32((1 + f/128) / 448) * 2^e exactly, and
-// the reciprocal brackets scale by 2^-e in the same way (scaling by a power
-// of two commutes with rounding while everything stays normal).  So the
-// 128 values fl32((1 + f/128) / 448) and their reciprocal brackets are
-// computed once per block with the IEEE intrinsics and the per-group work
-// is an exponent add.  Zero, subnormal or huge absmax values take
-// make_divisor.
+// RN(1/s) scales by 2^-e in the same way (scaling by a power of two
+// commutes with rounding while everything stays normal).  So the 128
+// values fl32((1 + f/128) / 448) and their reciprocals are computed once
+// per block with the IEEE intrinsics and the per-group work is an exponent
+// add.  Absmax values outside the range where s >= 2^-93 and 1/s is normal
+// take make_divisor.
 struct DivTable {
-  uint32_t s[128];     // bits of fl32((1 + f/128) / 448)
-  uint32_t rlo[128];   // bits of RD(1 / s)
-  uint32_t rup[128];   // bits of RU(1 / s) + 2 ulps
+  uint32_t s[128];  // bits of fl32((1 + f/128) / 448)
+  uint32_t y[128];  // bits of RN(1 / s)
 };
 
 __device__ __forceinline__ void div_table_init(DivTable& t) {
   for (int f = threadIdx.x; f < 128; f += blockDim.x) {
     const float sf = __fdiv_rn(1.0f + static_cast<float>(f) * (1.0f / 128.0f), kE4M3Max);
-    const float lo = __frcp_rd(sf);
     t.s[f] = __float_as_uint(sf);
-    t.rlo[f] = __float_as_uint(lo);
-    t.rup[f] = __float_as_uint(recip_up(lo, sf));
+    t.y[f] = __float_as_uint(__frcp_rn(sf));
   }
 }
 
 // absmax given as BF16 bits (non-negative).
 __device__ __forceinline__ Divisor table_divisor(const DivTable& t, uint32_t a16) {
   const uint32_t e = a16 >> 7;  // biased exponent of the absmax
-  // the scale (about 2^(e-127) / 448) and the reciprocals stay normal for
-  // biased exponents 10..254 of the absmax
-  if (e < 10 || e > 254) return make_divisor(__uint_as_float(a16 << 16));
+  // biased exponents 43..254 give s >= 2^-93 with a normal reciprocal
+  if (e < 43 || e > 254) return make_divisor(__uint_as_float(a16 << 16));
   const uint32_t f = a16 & 0x7Fu;
   const int sh = static_cast<int>(e) - 127;
   Divisor d;
   d.s = __uint_as_float(t.s[f] + (static_cast<uint32_t>(sh) << 23));
-  d.r_lo = __uint_as_float(t.rlo[f] - (static_cast<uint32_t>(sh) << 23));
-  d.r_up = __uint_as_float(t.rup[f] - (static_cast<uint32_t>(sh) << 23));
+  d.y = __uint_as_float(t.y[f] - (static_cast<uint32_t>(sh) << 23));
   d.fast = true;
   return d;
 }
 
 // Power-of-two ("rounded") scale, §3.3.3 "low-precision activations" (1):
 // s = 2^k, the smallest power of two with absmax / s <= 448, k >= -149 (the
-// smallest positive float32).  x / s is then exact, so the bracket is a
-// single exact product (r_lo = r_up = 2^-k) whenever 2^-k is a normal
-// float32; scales below 2^-127 take the exact division path.
+// smallest positive float32).  y = 2^-k is then exact and so is x * y (the
+// correction term vanishes); the same s >= 2^-93 bound as for any divisor
+// selects the fast path.
 __device__ __forceinline__ Divisor pow2_from_exp(int k) {
   k = max(k, -149);
   Divisor d;
   d.s = k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23) : __uint_as_float(1u << (k + 149));
-  d.fast = k >= -127 && k <= 126;
-  const float r = d.fast ? __uint_as_float(static_cast<uint32_t>(127 - k) << 23) : 1.0f;
-  d.r_lo = r;
-  d.r_up = r;
+  d.fast = k >= -93 && k <= 126;
+  d.y = d.fast ? __uint_as_float(static_cast<uint32_t>(127 - k) << 23) : 1.0f;
   return d;
 }
 
@@ -114,7 +106,7 @@ __device__ __forceinline__ Divisor pow2_divisor_f32(float a) {
   if (!(a > 0.0f)) {
     Divisor d;
     d.s = 0.0f;
-    d.r_lo = d.r_up = 1.0f;
+    d.y = 1.0f;
     d.fast = false;
     return d;
   }
@@ -164,46 +156,39 @@ __device__ __forceinline__ uint32_t absmax8_bits(uint4 v) {
   return abs_bits(absmax_step(absmax_step(v.x, v.y), absmax_step(v.z, v.w)));
 }
 
-// Eight consecutive values of one group -> eight codes (byte i = value i),
-// without a division per element.  With signed products truncated toward
-// zero,
-//   |RZ(x * r_lo)| <= |x| / s <= |RZ(x * r_up)|,
-// both of x's sign, so the correctly rounded quotient fl32(x / s) lies
-// between them.  Rounding to E4M3 (RNE, saturating) is monotonic and odd,
-// hence when both ends give the same code (sign included), so does
-// fl32(x / s).  When an E4M3 rounding boundary falls inside the few-ulp
-// wide bracket, or s is not a normal float, bit j of `badmask` is set for
-// the pair (values 2j, 2j+1) and the caller redoes it with quant2_exact.
-__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float2 rlo, float2 rup, uint32_t& bad) {
+// Codes of the BF16 pair w (low half first) in bits 0..15, by the
+// Markstein quotient (see Divisor); ns2 = (-s, -s), y2 = (y, y).  The sign of
+// a -0 input is restored by the caller (signs4).
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float2 y2, float2 ns2) {
   const float2 a = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-  const float2 l = __fmul2_rz(a, rlo);
-  const float2 u = __fmul2_rz(a, rup);
-  const uint32_t c = e4m3x2(l.x, l.y);
-  bad = c != e4m3x2(u.x, u.y) ? 1u : 0u;
-  return c;
+  const float2 q0 = __fmul2_rn(a, y2);
+  const float2 r = __ffma2_rn(q0, ns2, a);
+  const float2 q1 = __ffma2_rn(r, y2, q0);
+  return e4m3x2(q1.x, q1.y);
 }
 
-__device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d, uint32_t& badmask) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
-  uint32_t c[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t b;
-    c[j] = quant_pair(w[j], rlo, rup, b);
-    badmask |= (b | (d.fast ? 0u : 1u)) << j;
-  }
-  return d.s == 0.0f ? make_uint2(0u, 0u) : make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+// Sign bits of the four BF16 values in words w0, w1 at bit 7 of the code
+// bytes they map to (byte i = value i).
+__device__ __forceinline__ uint32_t signs4(uint32_t w0, uint32_t w1) {
+  return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
 }
 
 // Codes of one value pair through IEEE divisions (x / s, then E4M3, sign
-// from the quotient): the exact path for a pair whose bracket straddles an
-// E4M3 rounding boundary.  Quotients of BF16 values close to such a
-// boundary are common (about 0.4% of the values of normal data), so the
-// fix-up is done per pair.
+// from the quotient): groups whose scale is below 2^-93 or zero.
 __device__ __forceinline__ uint32_t quant2_exact(uint32_t w, float s) {
   if (s == 0.0f) return 0u;
   return e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
+}
+
+// Eight consecutive values of one group -> eight codes (byte i = value i).
+__device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d) {
+  if (!d.fast)
+    return make_uint2(quant2_exact(v.x, d.s) | (quant2_exact(v.y, d.s) << 16),
+                      quant2_exact(v.z, d.s) | (quant2_exact(v.w, d.s) << 16));
+  const float2 y2 = make_float2(d.y, d.y), ns2 = make_float2(-d.s, -d.s);
+  const uint32_t c0 = quant_pair(v.x, y2, ns2), c1 = quant_pair(v.y, y2, ns2);
+  const uint32_t c2 = quant_pair(v.z, y2, ns2), c3 = quant_pair(v.w, y2, ns2);
+  return make_uint2(__byte_perm(c0, c1, 0x5410) | signs4(v.x, v.y), __byte_perm(c2, c3, 0x5410) | signs4(v.z, v.w));
 }
 
 // Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
@@ -282,7 +267,6 @@ struct QShared {
   uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
   uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
   uint32_t colmax[kGroup / 2];                         // dual: column maxima of the tile, two per word
-  uint32_t rowabs[kGroup];                             // dual: row maxima of the tile (BF16 bits)
 };
 
 template <int kMode>
@@ -313,38 +297,11 @@ __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, 256;" 
 __device__ __forceinline__ uint32_t umax_halves(uint32_t m) { return umax16x2(m, __byte_perm(m, 0u, 0x1032)); }
 
 // Row layout: quantises the thread's 64 values (32 words in load order) with
-// one divisor, stores the 64 codes, then fixes the value pairs whose bracket
-// was inconclusive with IEEE divisions (about 0.4% of values: each lane
-// walks its own flagged pairs after the bulk store, instead of every lane
-// of a warp stepping through every lane's fix-ups).
-__device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divisor& d, int h, const uint8_t* rowp,
-                                            int rsw, uint8_t* out) {
-  if (!d.fast) {
-    // s == 0 (all-zero group) or a subnormal s: exact path for every value
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = (i + 4 * h) & 7;
-      uint2 c;
-      c.x = quant2_exact(w[4 * i], d.s) | (quant2_exact(w[4 * i + 1], d.s) << 16);
-      c.y = quant2_exact(w[4 * i + 2], d.s) | (quant2_exact(w[4 * i + 3], d.s) << 16);
-      *reinterpret_cast<uint2*>(out + 8 * j) = c;
-    }
-    return;
-  }
-  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
+// one divisor and stores the 64 codes as four 16-byte writes.
+__device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divisor& d, int h, uint8_t* out) {
   uint2 cc[8];
-  uint32_t bm = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t c[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t b;
-      c[k] = quant_pair(w[4 * i + k], rlo, rup, b);
-      bm |= b << (4 * i + k);
-    }
-    cc[i] = make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
-  }
+  for (int i = 0; i < 8; ++i) cc[i] = quant8m(make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]), d);
   // load order -> column order: the upper half started at chunk 4
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -355,13 +312,6 @@ __device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divis
 #pragma unroll
   for (int p = 0; p < 4; ++p)
     *reinterpret_cast<uint4*>(out + 16 * p) = make_uint4(cc[2 * p].x, cc[2 * p].y, cc[2 * p + 1].x, cc[2 * p + 1].y);
-  while (bm != 0u) {
-    const int k = __ffs(bm) - 1;
-    bm &= bm - 1u;
-    const int j = ((k >> 2) + 4 * h) & 7;  // logical chunk of word k
-    const uint32_t wk = *reinterpret_cast<const uint32_t*>(rowp + (((j ^ rsw) << 4) | ((k & 3) << 2)));
-    *reinterpret_cast<uint16_t*>(out + 8 * j + 2 * (k & 3)) = static_cast<uint16_t>(quant2_exact(wk, d.s));
-  }
 }
 
 template <int kMode>
@@ -438,7 +388,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
     const uint8_t* stage = tiles + s * kTileBytes;
 
     if (Q::kRowLayout) {
-      const int r = t >> 1, h = t & 1, rsw = r & 7;
+      const int r = t >> 1, h = t & 1, rsw = r & 7;  // 128-byte swizzle: chunk i of row r at i ^ (r % 8)
       const uint8_t* rowp = stage + h * (kTileBytes / 2) + r * 128;
       uint32_t w[32];
 #pragma unroll
@@ -450,6 +400,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
       }
+      // the tile is in registers: hand the stage back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+      if (++s == Q::kStages) { s = 0; ph ^= 1u; }
       uint32_t m = w[0];
 #pragma unroll
       for (int k = 1; k < 32; ++k) m = absmax_step(m, w[k]);
@@ -478,10 +432,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         d = group_divisor(S.tab, m & 0xFFFFu, p.pow2 != 0);
         if (h == 0 && row < p.rows) p.s[static_cast<int64_t>(kb) * p.rows + row] = d.s;
       }
-      if (row < p.rows) quant_row64(w, d, h, rowp, rsw, p.q + row * K + static_cast<int64_t>(kb) * kGroup + 64 * h);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[s]);
-      if (++s == Q::kStages) { s = 0; ph ^= 1u; }
+      if (row < p.rows) quant_row64(w, d, h, p.q + row * K + static_cast<int64_t>(kb) * kGroup + 64 * h);
       continue;
     }
 
@@ -495,7 +446,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       v[j] = ok ? *reinterpret_cast<const uint4*>(src + j * kTileRowBytes) : make_uint4(0u, 0u, 0u, 0u);
     const int64_t r0 = rb * kGroup + 8 * g;                        // this thread's first row
     const int64_t c0 = static_cast<int64_t>(kb) * kGroup + 8 * c;  // and first column
-    uint32_t rowbad = 0;  // bit 4j+k: pair k of row j needs the exact path
+    // the tile is in registers: hand the stage back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (++s == Q::kStages) { s = 0; ph ^= 1u; }
 
     if (kMode == kModeWeightT) {
       uint32_t m = 0;
@@ -520,23 +474,12 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       uint2 q[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t bm = 0;
-        q[j] = quant8m(v[j], d, bm);
-        rowbad |= bm << (4 * j);
+        q[j] = quant8m(v[j], d);
         *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q[j];
       }
       // one scale for the block: the codes of W^T are the transposed codes
 #pragma unroll
       for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = byte_column(q, i);
-      while (rowbad != 0u) {
-        const int b = __ffs(rowbad) - 1;
-        rowbad &= rowbad - 1u;
-        const int j = b >> 2, k = b & 3;
-        const uint32_t e = quant2_exact(*reinterpret_cast<const uint32_t*>(src + j * kTileRowBytes + 4 * k), d.s);
-        *reinterpret_cast<uint16_t*>(p.q + (r0 + j) * K + c0 + 2 * k) = static_cast<uint16_t>(e);
-        p.q_t[(c0 + 2 * k) * p.rows + r0 + j] = static_cast<uint8_t>(e);
-        p.q_t[(c0 + 2 * k + 1) * p.rows + r0 + j] = static_cast<uint8_t>(e >> 8);
-      }
     } else {
       // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
       // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
@@ -547,21 +490,11 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 #pragma unroll
         for (int o = 1; o <= 8; o <<= 1) am[i] = umax16x2(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
       }
-      if (c == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          S.rowabs[8 * g + 2 * i] = am[i] & 0xFFFFu;
-          S.rowabs[8 * g + 2 * i + 1] = am[i] >> 16;
-        }
-      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
         const Divisor d = group_divisor(S.tab, a16, p.pow2 != 0);
-        uint32_t bm = 0;
-        const uint2 q = quant8m(v[j], d, bm);
-        rowbad |= bm << (4 * j);
-        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q;
+        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = quant8m(v[j], d);
         if (c == 0) p.s[static_cast<int64_t>(kb) * p.rows + r0 + j] = d.s;
       }
       // 128x1 groups: transpose the 8x8 sub-block (column i of the tile
@@ -602,39 +535,13 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         st[1] = group_divisor(S.tab, m >> 16, p.pow2 != 0).s;
       }
       compute_bar();
-      uint32_t colbad = 0;  // bit 4i+m: rows 2m, 2m+1 of column i need the exact path
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t m = S.colmax[4 * c + (i >> 1)];
         const Divisor d = group_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
-        uint32_t bm = 0;
-        const uint2 q = quant8m(vt[i], d, bm);
-        colbad |= bm << (4 * i);
-        *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = q;
-      }
-      while (rowbad != 0u) {
-        const int b = __ffs(rowbad) - 1;
-        rowbad &= rowbad - 1u;
-        const int j = b >> 2, k = b & 3;
-        const float sj = group_divisor(S.tab, S.rowabs[8 * g + j], p.pow2 != 0).s;
-        const uint32_t e = quant2_exact(*reinterpret_cast<const uint32_t*>(src + j * kTileRowBytes + 4 * k), sj);
-        *reinterpret_cast<uint16_t*>(p.q + (r0 + j) * K + c0 + 2 * k) = static_cast<uint16_t>(e);
-      }
-      while (colbad != 0u) {
-        const int b = __ffs(colbad) - 1;
-        colbad &= colbad - 1u;
-        const int i = b >> 2, m = b & 3;
-        const uint32_t cm = S.colmax[4 * c + (i >> 1)];
-        const float si = group_divisor(S.tab, (i & 1) ? (cm >> 16) : (cm & 0xFFFFu), p.pow2 != 0).s;
-        const uint16_t* col = reinterpret_cast<const uint16_t*>(src + 2 * m * kTileRowBytes) + i;
-        const uint32_t wd = static_cast<uint32_t>(col[0]) | (static_cast<uint32_t>(col[kTileRowBytes / 2]) << 16);
-        *reinterpret_cast<uint16_t*>(p.q_t + (c0 + i) * p.rows + r0 + 2 * m) =
-            static_cast<uint16_t>(quant2_exact(wd, si));
+        *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = quant8m(vt[i], d);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
-    if (++s == Q::kStages) { s = 0; ph ^= 1u; }
   }
 }
 
@@ -703,21 +610,27 @@ struct RequantParams {
   int pow2;
 };
 
-// Eight float32 values -> eight codes with one divisor (bracketed products,
-// as quant_pair); bit j of `bad` flags pair j for the exact path.
-__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d, uint32_t& bad) {
-  const float2 rlo = make_float2(d.r_lo, d.r_lo), rup = make_float2(d.r_up, d.r_up);
+// Eight float32 values -> eight codes with one divisor (Markstein quotients
+// as quant_pair; IEEE divisions for a slow divisor; the sign bit of each
+// input ORed into its code to keep the sign of -0).
+__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d) {
   uint32_t c[4];
-  bad = 0;
+  if (!d.fast) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
-    const float2 l = __fmul2_rz(a, rlo);
-    const float2 u = __fmul2_rz(a, rup);
-    c[j] = e4m3x2(l.x, l.y);
-    bad |= ((c[j] != e4m3x2(u.x, u.y)) || !d.fast ? 1u : 0u) << j;
+    for (int j = 0; j < 4; ++j)
+      c[j] = d.s == 0.0f ? 0u : e4m3x2(__fdiv_rn(v[2 * j], d.s), __fdiv_rn(v[2 * j + 1], d.s));
+  } else {
+    const float2 y2 = make_float2(d.y, d.y), ns2 = make_float2(-d.s, -d.s);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
+      const float2 q0 = __fmul2_rn(a, y2);
+      const float2 r = __ffma2_rn(q0, ns2, a);
+      const float2 q1 = __ffma2_rn(r, y2, q0);
+      c[j] = e4m3x2(q1.x, q1.y) |
+             (__byte_perm(__float_as_uint(v[2 * j]), __float_as_uint(v[2 * j + 1]), 0x0073) & 0x8080u);
+    }
   }
-  if (d.s == 0.0f) return make_uint2(0u, 0u);
   return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
 }
 
@@ -791,19 +704,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const Divisor d = divisor_f32(colmax[8 * c + i], p.pow2 != 0);
-      uint32_t bad;
-      uint2 code = quant8f(v[i], d, bad);
-      if (bad != 0u) {  // pairs whose bracket straddles an E4M3 rounding boundary: IEEE divisions
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (!(bad & (1u << k))) continue;
-          const uint32_t e =
-              d.s == 0.0f ? 0u : e4m3x2(__fdiv_rn(v[i][2 * k], d.s), __fdiv_rn(v[i][2 * k + 1], d.s));
-          uint32_t& word = k < 2 ? code.x : code.y;
-          const int sh = 16 * (k & 1);
-          word = (word & ~(0xFFFFu << sh)) | (e << sh);
-        }
-      }
+      const uint2 code = quant8f(v[i], d);
       *reinterpret_cast<uint2*>(p.xq_t + (static_cast<int64_t>(kb) * kGroup + 8 * c + i) * p.M + r0) = code;
     }
   }
