@@ -641,43 +641,47 @@ __device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
 __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantParams p) {
   __shared__ uint32_t colred[kRqThreads / 32][kGroup];  // per-warp column maxima (|v| bits)
   __shared__ float colmax[kGroup];
+  // Output tile: row R of X^T's tile (tile column R) as 16 units of 8 codes;
+  // unit u of row R is stored at u ^ (R / 8), so the 8-byte writes of a warp
+  // (16 rows R = 8c+i, one unit each) hit 16 different bank pairs.
+  __shared__ __align__(16) uint2 stg[kGroup][kGroup / 8];
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int g = t >> 4, c = t & 15;
   uint2 nq[8];
-  auto load = [&](int64_t tile, uint2 (&q)[8]) {
+  float4 ns[2];
+  auto load = [&](int64_t tile, uint2 (&q)[8], float4 (&sc)[2]) {
     if (tile >= p.ntiles) return;
     const int64_t rb = tile / p.nkb;
     const int kb = static_cast<int>(tile - rb * p.nkb);
     const uint8_t* src = p.xq + (rb * kGroup + 8 * g) * p.K + static_cast<int64_t>(kb) * kGroup + 8 * c;
 #pragma unroll
     for (int j = 0; j < 8; ++j) q[j] = __ldg(reinterpret_cast<const uint2*>(src + j * p.K));
+    const float4* sp = reinterpret_cast<const float4*>(p.sx + static_cast<int64_t>(kb) * p.M + rb * kGroup + 8 * g);
+    sc[0] = __ldg(sp);
+    sc[1] = __ldg(sp + 1);
   };
-  load(blockIdx.x, nq);
+  load(blockIdx.x, nq, ns);
   for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-    uint2 q[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = nq[j];
-    load(tile + gridDim.x, nq);
-    const int64_t rb = tile / p.nkb;
-    const int kb = static_cast<int>(tile - rb * p.nkb);
-    const int64_t r0 = rb * kGroup + 8 * g;
-    const float4 s_lo = __ldg(reinterpret_cast<const float4*>(p.sx + static_cast<int64_t>(kb) * p.M + r0));
-    const float4 s_hi = __ldg(reinterpret_cast<const float4*>(p.sx + static_cast<int64_t>(kb) * p.M + r0 + 4));
-    const float sr[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
     // dequantise: v[i][j] = column i, row j of the thread's 8x8 sub-block
     float v[8][8];
+    {
+      const float sr[8] = {ns[0].x, ns[0].y, ns[0].z, ns[0].w, ns[1].x, ns[1].y, ns[1].z, ns[1].w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t w2[2] = {q[j].x, q[j].y};
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w2[2] = {nq[j].x, nq[j].y};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
-            static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu), __NV_E4M3);
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        v[2 * h][j] = __fmul_rn(f.x, sr[j]);
-        v[2 * h + 1][j] = __fmul_rn(f.y, sr[j]);
+        for (int h = 0; h < 4; ++h) {
+          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+              static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu), __NV_E4M3);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+          v[2 * h][j] = __fmul_rn(f.x, sr[j]);
+          v[2 * h + 1][j] = __fmul_rn(f.y, sr[j]);
+        }
       }
     }
+    load(tile + gridDim.x, nq, ns);  // the next tile's codes and scales are in flight meanwhile
+    const int64_t rb = tile / p.nkb;
+    const int kb = static_cast<int>(tile - rb * p.nkb);
     // column maxima of |v| (non-negative floats order like their bits)
     uint32_t m[8];
 #pragma unroll
@@ -704,8 +708,18 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const Divisor d = divisor_f32(colmax[8 * c + i], p.pow2 != 0);
-      const uint2 code = quant8f(v[i], d);
-      *reinterpret_cast<uint2*>(p.xq_t + (static_cast<int64_t>(kb) * kGroup + 8 * c + i) * p.M + r0) = code;
+      stg[8 * c + i][g ^ c] = quant8f(v[i], d);
+    }
+    __syncthreads();
+    // write the tile out: 8 threads per 128-byte row of X^T
+#pragma unroll
+    for (int it = 0; it < kGroup * kGroup / 16 / kRqThreads; ++it) {
+      const int idx = it * kRqThreads + t;
+      const int R = idx >> 3, k = idx & 7, cr = R >> 3;
+      uint4 w = *reinterpret_cast<const uint4*>(&stg[R][2 * k]);
+      if (cr & 1) w = make_uint4(w.z, w.w, w.x, w.y);
+      const int kl = k ^ (cr >> 1);  // logical 16-byte chunk of the row
+      *reinterpret_cast<uint4*>(p.xq_t + (static_cast<int64_t>(kb) * kGroup + R) * p.M + rb * kGroup + 16 * kl) = w;
     }
   }
 }
