@@ -238,7 +238,10 @@ enum TileMode : int {
 template <int kMode>
 struct QCfg {
   static constexpr bool kRowLayout = kMode == kModeAct || kMode == kModeWeight;
-  static constexpr int kStages = 3;
+  // block layouts also stage the transposed codes of a tile (16 KB) in
+  // shared memory; two input stages keep two CTAs per SM
+  static constexpr int kStages = kRowLayout ? 3 : 2;
+  static constexpr int kStageOutBytes = kRowLayout ? 0 : kGroup * kGroup;
   static constexpr int kMinBlocks = 2;  // CTAs per SM the registers and shared memory are budgeted for
 };
 
@@ -271,7 +274,7 @@ struct QShared {
 
 template <int kMode>
 constexpr int q_smem_bytes() {
-  return QCfg<kMode>::kStages * kTileBytes + static_cast<int>(sizeof(QShared)) + 1024;
+  return QCfg<kMode>::kStages * kTileBytes + QCfg<kMode>::kStageOutBytes + static_cast<int>(sizeof(QShared)) + 1024;
 }
 
 __device__ int g_quant_status;
@@ -320,7 +323,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
   using Q = QCfg<kMode>;
   extern __shared__ uint8_t qsmem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
-  QShared& S = *reinterpret_cast<QShared*>(tiles + Q::kStages * kTileBytes);
+  // transposed codes of the current tile (block layouts): row R of the
+  // tile's X^T part as 16 units of 8 codes, unit u stored at u ^ (R / 8)
+  uint2 (*stg)[kGroup / 8] = reinterpret_cast<uint2 (*)[kGroup / 8]>(tiles + Q::kStages * kTileBytes);
+  QShared& S = *reinterpret_cast<QShared*>(tiles + Q::kStages * kTileBytes + Q::kStageOutBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = p.nrb * p.nkb;
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       }
       // one scale for the block: the codes of W^T are the transposed codes
 #pragma unroll
-      for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = byte_column(q, i);
+      for (int i = 0; i < 8; ++i) stg[8 * c + i][g ^ c] = byte_column(q, i);
     } else {
       // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
       // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
@@ -539,8 +545,19 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       for (int i = 0; i < 8; ++i) {
         const uint32_t m = S.colmax[4 * c + (i >> 1)];
         const Divisor d = group_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
-        *reinterpret_cast<uint2*>(p.q_t + (c0 + i) * p.rows + r0) = quant8m(vt[i], d);
+        stg[8 * c + i][g ^ c] = quant8m(vt[i], d);
       }
+    }
+    // write the staged transposed codes: 8 threads per 128-byte row
+    compute_bar();
+#pragma unroll
+    for (int it = 0; it < (Q::kRowLayout ? 0 : kGroup * kGroup / 16 / kQComputeThreads); ++it) {
+      const int idx = it * kQComputeThreads + t;
+      const int R = idx >> 3, k = idx & 7, cr = R >> 3;
+      uint4 w = *reinterpret_cast<const uint4*>(&stg[R][2 * k]);
+      if (cr & 1) w = make_uint4(w.z, w.w, w.x, w.y);
+      const int kl = k ^ (cr >> 1);  // logical 16-byte chunk of the row
+      *reinterpret_cast<uint4*>(p.q_t + (static_cast<int64_t>(kb) * kGroup + R) * p.rows + rb * kGroup + 16 * kl) = w;
     }
   }
 }
