@@ -140,3 +140,36 @@ def quantize_weight_128x128(w, pow2: bool = False):
     codes, s = quantize_groups(blocks, pow2)
     codes = codes.reshape(nb, kb, GROUP, GROUP).transpose(0, 2, 1, 3).reshape(N, K)
     return codes, s.reshape(nb, kb)
+
+
+def swiglu(h, inter: int) -> np.ndarray:
+    """SwiGLU of the MoE gate/up projection output, in float64.
+
+    DeepSeek-V3 §3.3.3 "low-precision activations" (2): the input of the
+    MoE SwiGLU operator is cached and its output recomputed; the output
+    feeds the down projection, whose input is quantised 1x128.  ``h`` is
+    [M, 2*inter] (BF16 bits or float32) with the gate projection in columns
+    [0, inter) and the up projection in [inter, 2*inter):
+        out = silu(gate) * up,   silu(g) = g / (1 + exp(-g)).
+    """
+    h = _as_f32(h).astype(np.float64)
+    g, u = h[:, :inter], h[:, inter:2 * inter]
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def bf16_round_f64(v) -> np.ndarray:
+    """Nearest BF16 value (ties to even) of float64 values, as float32; exact."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex.astype(np.int64) - 1, -126)    # BF16 shares float32's exponent range
+    quantum = np.exp2((e - 7).astype(np.float64))
+    r = np.rint(a / quantum) * quantum               # a / quantum is exact; rint: ties to even
+    return np.copysign(r, v).astype(np.float32)      # exact: r has <= 8 significant bits
+
+
+def swiglu_quantize_1x128(h, inter: int, pow2: bool = False):
+    """The 1x128 quantisation of the BF16-rounded SwiGLU output (the unfused
+    pipeline: SwiGLU -> BF16 activation -> 1x128 quantise)."""
+    return quantize_act_1x128(bf16_round_f64(swiglu(h, inter)), pow2)
