@@ -22,9 +22,9 @@ from .build import LIB_PATH, build as _build
 __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
-    "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1",
+    "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string",
-    "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1",
+    "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1", "swiglu_quantize",
     "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128", "SCALE_ABSMAX", "SCALE_POW2",
 ]
 
@@ -53,6 +53,7 @@ _SIGNATURES = {
     "fp8bs_quantize_act_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_quantize_weight_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_requant_1x128_to_128x1": [_c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
+    "fp8bs_swiglu_quantize": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_gemm": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
     "fp8bs_grouped_gemm": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                            _c_vp],
@@ -138,6 +139,12 @@ def fp8bs_requant_1x128_to_128x1(xq, sx, M, K, xq_t, sx_t, scale_mode=SCALE_POW2
                                             _stream(stream)), "fp8bs_requant_1x128_to_128x1")
 
 
+def fp8bs_swiglu_quantize(h, M, I, ldh, q, s, scale_mode=SCALE_ABSMAX, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_swiglu_quantize(_ptr(h), M, I, ldh, _ptr(q), _ptr(s), int(scale_mode), _stream(stream)),
+           "fp8bs_swiglu_quantize")
+
+
 def fp8bs_gemm(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate=0, stream=None):
     lib = load_library()
     _check(lib.fp8bs_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), sb_kind, _ptr(d), d_dtype, M, N, K,
@@ -195,6 +202,18 @@ def quantize_weight(w, transposed: bool = False, pow2: bool = False, stream=None
         sw_t = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
     fp8bs_quantize_weight_ex(w, N, K, w.stride(0), wq, sw, wq_t, sw_t, SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
     return (wq, sw, wq_t, sw_t) if transposed else (wq, sw)
+
+
+def swiglu_quantize(h, pow2: bool = False, stream=None):
+    """h: [M, 2I] bfloat16 CUDA tensor (gate | up).  Returns (q [M, I] uint8,
+    s [I/128, M] float32): the 1x128 quantisation of BF16(silu(gate) * up)."""
+    import torch
+    M, two_i = h.shape
+    I = two_i // 2
+    q = torch.empty((M, I), dtype=torch.uint8, device=h.device)
+    s = torch.empty((I // 128, M), dtype=torch.float32, device=h.device)
+    fp8bs_swiglu_quantize(h, M, I, h.stride(0), q, s, SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
+    return q, s
 
 
 def requant_1x128_to_128x1(xq, sx, pow2: bool = True, stream=None):

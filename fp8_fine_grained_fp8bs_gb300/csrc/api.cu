@@ -117,6 +117,23 @@ int fp8bs_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, 
                                                         static_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_swiglu_quantize(const void* h, int64_t M, int64_t I, int64_t ldh, uint8_t* q, float* s, int scale_mode,
+                          void* stream) {
+  if (M < 0 || I < 0 || ldh < 2 * I) return FP8BS_ERR_INVALID_ARG;
+  if (scale_mode != FP8BS_SCALE_ABSMAX && scale_mode != FP8BS_SCALE_POW2) return FP8BS_ERR_INVALID_ARG;
+  if (I % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) || I > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (M == 0 || I == 0) return FP8BS_OK;
+  if (h == nullptr || q == nullptr || s == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(q) || !aligned16(s) || (ldh * 2) % 16 != 0) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_swiglu_quantize(static_cast<const uint16_t*>(h), M, I, ldh, q, s,
+                                                 scale_mode == FP8BS_SCALE_POW2, sms,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 static int run_gemm(const fp8bs::GemmArgs& args, void* stream) {
   int sms = 0;
   const int st = current_device(&sms);

@@ -24,6 +24,10 @@ cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int6
 // plain loads, no waits.
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,
                                           float* sx_t, bool pow2, int sm_count, cudaStream_t stream);
+// Fused SwiGLU (gate columns [0, I), up columns [I, 2I) of h) and 1x128
+// quantisation of the BF16-rounded result; plain loads, no waits.
+cudaError_t launch_swiglu_quantize(const uint16_t* h, int64_t M, int64_t I, int64_t ldh, uint8_t* q, float* s,
+                                   bool pow2, int sm_count, cudaStream_t stream);
 // Reads and clears the quantisers' device status word (synchronous copy on
 // the current device).
 cudaError_t quant_take_status(int* status);

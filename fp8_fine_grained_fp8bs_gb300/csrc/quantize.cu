@@ -10,6 +10,7 @@
 // below), so every byte is read once and written once and no element needs
 // a division.
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -741,6 +742,79 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused SwiGLU -> 1x128 quantisation: the input of the MoE down projection
+// (§3.3.3 "low-precision activations" (2): the SwiGLU input is cached and
+// its output recomputed; the output feeds the FP8 down-projection GEMM).
+// Fusing the cast into the producer removes the BF16 write and re-read of
+// the SwiGLU output (the read-write-reread cost §3.5.2 names).  h [M][ldh]
+// BF16 holds the gate projection in columns [0, I) and the up projection in
+// [I, 2I).  Thread = 8 consecutive outputs of one row (16-byte loads of gate
+// and up, the next ones in flight); the 16 lanes of a half-warp are one
+// 1x128 group.  v = BF16_rne(silu(g) * u), silu(g) = g / (1 + exp(-g)) in
+// FP32 (fast exp and divide: relative error below 2^-16 for |g| <= 80), then
+// the group is quantised exactly as fp8bs_quantize_act does with a BF16
+// input.
+constexpr int kSgThreads = 256;
+
+struct SwigluParams {
+  const uint16_t* h;
+  int64_t ldh, M, I;
+  uint8_t* q;     // [M][I]
+  float* s;       // [I/128][M], kb-major
+  int64_t units;  // M * I / 8
+  int pow2;
+};
+
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw) {
+  const float g0 = __uint_as_float(gw << 16), g1 = __uint_as_float(gw & 0xFFFF0000u);
+  const float u0 = __uint_as_float(uw << 16), u1 = __uint_as_float(uw & 0xFFFF0000u);
+  const float v0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+  const float v1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v0, v1);  // v0 in the low half
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluParams p) {
+  __shared__ DivTable tab;
+  div_table_init(tab);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t upr = p.I / 8;                                   // units (8 outputs) per row
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSgThreads;
+  // Loop bounds are per warp (a multiple of 32 units); units come in whole
+  // groups of 16, so a half-warp is entirely in or out of range.
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kSgThreads + (threadIdx.x & ~31);
+  uint4 ng = make_uint4(0u, 0u, 0u, 0u), nu = ng;
+  auto load = [&](int64_t u, uint4& g, uint4& up) {
+    if (u >= p.units) return;
+    const int64_t m = u / upr, c = u - m * upr;
+    const uint16_t* row = p.h + m * p.ldh + c * 8;
+    g = __ldg(reinterpret_cast<const uint4*>(row));
+    up = __ldg(reinterpret_cast<const uint4*>(row + p.I));
+  };
+  load(first + lane, ng, nu);
+  for (int64_t base = first; base < p.units; base += stride) {
+    const int64_t u = base + lane;
+    const uint4 g = ng, up = nu;
+    load(u + stride, ng, nu);
+    uint4 v;
+    v.x = swiglu_pair(g.x, up.x);
+    v.y = swiglu_pair(g.y, up.y);
+    v.z = swiglu_pair(g.z, up.z);
+    v.w = swiglu_pair(g.w, up.w);
+    uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
+#pragma unroll
+    for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));  // the 16 lanes of a group
+    const Divisor d = group_divisor(tab, m, p.pow2 != 0);
+    if (u < p.units) {
+      const int64_t row = u / upr, c = u - row * upr;
+      *reinterpret_cast<uint2*>(p.q + row * p.I + c * 8) = quant8m(v, d);
+      if ((c & 15) == 0) p.s[(c >> 4) * p.M + row] = d.s;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
@@ -787,6 +861,31 @@ cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, in
   }
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   requant_kernel<<<static_cast<int>(p.ntiles < slots ? p.ntiles : slots), kRqThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quantize(const uint16_t* h, int64_t M, int64_t I, int64_t ldh, uint8_t* q, float* s,
+                                   bool pow2, int sm_count, cudaStream_t stream) {
+  SwigluParams p;
+  p.h = h;
+  p.ldh = ldh;
+  p.M = M;
+  p.I = I;
+  p.q = q;
+  p.s = s;
+  p.units = M * (I / 8);
+  p.pow2 = pow2 ? 1 : 0;
+  if (p.units <= 0) return cudaSuccess;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_quant_kernel, kSgThreads, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const int64_t need = (p.units + kSgThreads - 1) / kSgThreads;
+  const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+  swiglu_quant_kernel<<<static_cast<int>(need < slots ? need : slots), kSgThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -151,6 +151,26 @@ int fp8bs_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, 
                                  uint8_t* xq_t, float* sx_t, int scale_mode, void* stream);
 
 /*
+ * Fused SwiGLU and 1x128 quantisation: the input of the MoE down projection
+ * (§3.3.3 "low-precision activations" (2): the SwiGLU output feeds the
+ * down-projection FP8 GEMM; doing the cast in the producer avoids writing and
+ * re-reading the BF16 activation, the cost §3.5.2 names):
+ *
+ *   v[m][i] = BF16_rne( silu(h[m][i]) * h[m][I + i] ),  silu(g) = g / (1 + e^-g)
+ *   (xq, sx) = the 1x128 quantisation of v, as fp8bs_quantize_act(_ex).
+ *
+ *   h   [M][ldh] BF16: the gate/up projection output, gate in columns [0, I),
+ *       up in columns [I, 2I).                                        (in)
+ *   q   [M][I] E4M3 codes.  s [I/128][M] float32, kb-major.            (out)
+ * silu is evaluated in FP32 with a relative error below 2^-16 for |gate| <= 80,
+ * so a value within that distance of a BF16 rounding boundary may round either
+ * way; codes and scales are otherwise those of quantising the rounded v.
+ * Rules: I % 128 == 0, ldh >= 2*I, ldh*2 % 16 == 0; pointers 16-byte aligned.
+ */
+int fp8bs_swiglu_quantize(const void* h, int64_t M, int64_t I, int64_t ldh,
+                          uint8_t* q, float* s, int scale_mode, void* stream);
+
+/*
  * Block-scaled FP8 GEMM, D = A * B^T with per-128-K-block dequantisation
  * (§3.3.2 "increasing accumulation precision", Figure 7b; Figure 7 explainer
  * formula out += MMA(FP8(x), FP8(w)) * s_x * s_w):

@@ -84,6 +84,17 @@ def test_scale_mode_and_requant_argument_errors(lib):
     assert rq(None, None, 0, 128, None, None, 1, None) == 0                       # empty: no-op
 
 
+def test_swiglu_quantize_argument_errors(lib):
+    sq = lib.fp8bs_swiglu_quantize
+    assert sq(FAKE, 128, 256, 384, FAKE, FAKE, 0, None) == 1                      # ldh < 2I
+    assert sq(FAKE, 128, 192, 384, FAKE, FAKE, 0, None) == 2                      # I % 128
+    assert sq(FAKE, 128, 128, 256, FAKE, FAKE, 7, None) == 1                      # scale mode
+    assert sq(FAKE, 128, 128, 260, FAKE, FAKE, 0, None) == 3                      # ldh * 2 % 16
+    assert sq(FAKE + 4, 128, 128, 256, FAKE, FAKE, 0, None) == 3
+    assert sq(None, 128, 128, 256, FAKE, FAKE, 0, None) == 1
+    assert sq(None, 0, 128, 256, None, None, 0, None) == 0                        # empty: no-op
+
+
 def test_gemm_argument_errors(lib):
     g = lib.fp8bs_gemm
     assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 100, 0, None) == 2   # K % 128
