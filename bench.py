@@ -19,7 +19,8 @@ run and reported beside it:
                   MoE grouped GEMMs (gate/up and down), dgrad, wgrad, the
                   dual-layout (1x128 + 128x1) activation quantize, the
                   weight quantize with its transposed copy, the power-of-two
-                  scale quantize and the FP8 1x128 -> 128x1 re-tiling.
+                  scale quantize, the FP8 1x128 -> 128x1 re-tiling and the
+                  fused SwiGLU -> 1x128 quantize of the MoE gate/up output.
 
 Multi-GPU: every rank runs its own replica on its own batch (data
 parallel, no collective on the data path); ``value`` sums all ranks' FLOPs
@@ -322,7 +323,14 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                                                    stream), stream, warmup, reps)
     out["moe_gate_up"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
                                    shape=f"grouped 32 experts, [{rows} x {2 * I} x {H}], BF16 out")
-    del aq, sa, bq, sb, y1, x_rows, w_gu
+    # fused SwiGLU -> 1x128 quantise of the gate/up output (the down projection's input)
+    sq = torch.empty((rows, I), dtype=torch.uint8, device=dev)
+    ss = torch.empty((I // 128, rows), dtype=torch.float32, device=dev)
+    ms = _time_ms(lambda: fp8bs.fp8bs_swiglu_quantize(y1, rows, I, 2 * I, sq, ss, fp8bs.SCALE_ABSMAX, stream),
+                  stream, warmup, reps)
+    out["swiglu_quantize"] = bw_line(rows * (2 * I * 2 + I + (I // 128) * 4), ms,
+                                     shape=f"[{rows} x {2 * I}] BF16 gate|up -> SwiGLU -> 1x128 E4M3 [{rows} x {I}]")
+    del aq, sa, bq, sb, y1, x_rows, w_gu, sq, ss
     aq, sa = fp8bs.quantize_act(d_in)
     bq, sb = fp8bs.quantize_weight(w_dn)
     y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
