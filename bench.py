@@ -288,6 +288,20 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                                                   "requantise), power-of-two scales")
     del dy, x, dyq_t, sdy_t, xq, sx, xq_t, sx_t, dw
 
+    # ---- context only (not part of the path): the library BF16 GEMM on the
+    # dense fprop shape, to set the "FP8 ~ 2x BF16" claim of the pages beside
+    # the block-scaled FP8 GEMM
+    g0 = torch.Generator(device=dev)
+    g0.manual_seed(2000 + rank)
+    xa = torch.randn((4096, 7168), generator=g0, device=dev).to(torch.bfloat16)
+    wa = (torch.randn((7168, 7168), generator=g0, device=dev) * 0.02).to(torch.bfloat16)
+    ya = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+    ms = _time_ms(lambda: torch.matmul(xa, wa.t(), out=ya), stream, warmup, reps)
+    out["context_bf16_matmul"] = gemm_line(2.0 * 4096 * 7168 * 7168, ms,
+                                           shape="torch.matmul BF16 4096x7168x7168 (cuBLAS), context only")
+    out["context_bf16_matmul"]["frac_of_bf16_peak"] = out["context_bf16_matmul"]["tflops"] / (fp8_peak / 2.0)
+    del xa, wa, ya
+
     # ---- weight quantize with the transposed copy
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + rank)
