@@ -388,9 +388,18 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
   const int t = threadIdx.x;
   int s = 0;
   uint32_t ph = 0, par = 0;
+  // (row block, column block) of the tile, advanced by the grid stride
+  // without a division per tile
+  const int64_t step_rb = static_cast<int64_t>(gridDim.x) / p.nkb;
+  const int step_kb = static_cast<int>(gridDim.x - step_rb * p.nkb);
+  int64_t rb = static_cast<int64_t>(blockIdx.x) / p.nkb;
+  int kb = static_cast<int>(blockIdx.x - rb * p.nkb);
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, par ^= 1u) {
-    const int64_t rb = tile / p.nkb;
-    const int kb = static_cast<int>(tile - rb * p.nkb);
+    if (tile != blockIdx.x) {
+      rb += step_rb;
+      kb += step_kb;
+      if (kb >= p.nkb) { kb -= p.nkb; ++rb; }
+    }
     const bool ok = mbar_wait(&S.full[s], ph, p.timeout_ns);
     const uint8_t* stage = tiles + s * kTileBytes;
 
@@ -762,7 +771,7 @@ struct SwigluParams {
   int64_t ldh, M, I;
   uint8_t* q;     // [M][I]
   float* s;       // [I/128][M], kb-major
-  int64_t units;  // M * I / 8
+  int64_t units;  // M * I / 8 (zero: nothing to do)
   int pow2;
 };
 
@@ -779,38 +788,37 @@ __global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluPa
   __shared__ DivTable tab;
   div_table_init(tab);
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t upr = p.I / 8;                                   // units (8 outputs) per row
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSgThreads;
-  // Loop bounds are per warp (a multiple of 32 units); units come in whole
-  // groups of 16, so a half-warp is entirely in or out of range.
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kSgThreads + (threadIdx.x & ~31);
-  uint4 ng = make_uint4(0u, 0u, 0u, 0u), nu = ng;
-  auto load = [&](int64_t u, uint4& g, uint4& up) {
-    if (u >= p.units) return;
-    const int64_t m = u / upr, c = u - m * upr;
-    const uint16_t* row = p.h + m * p.ldh + c * 8;
-    g = __ldg(reinterpret_cast<const uint4*>(row));
-    up = __ldg(reinterpret_cast<const uint4*>(row + p.I));
-  };
-  load(first + lane, ng, nu);
-  for (int64_t base = first; base < p.units; base += stride) {
-    const int64_t u = base + lane;
-    const uint4 g = ng, up = nu;
-    load(u + stride, ng, nu);
-    uint4 v;
-    v.x = swiglu_pair(g.x, up.x);
-    v.y = swiglu_pair(g.y, up.y);
-    v.z = swiglu_pair(g.z, up.z);
-    v.w = swiglu_pair(g.w, up.w);
-    uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
+  // Thread -> (row of a block of R rows, unit of that row); the units of a
+  // row come in whole groups of 16, so every half-warp is one 1x128 group and
+  // is entirely active or idle: shuffles use half-warp masks.  Rows with more
+  // than 256 units are walked in steps of 256.  No per-element integer
+  // division: the mapping is set up once.
+  const int t = threadIdx.x;
+  const int upr = static_cast<int>(p.I / 8);              // units (8 outputs) per row, a multiple of 16
+  const int R = upr <= kSgThreads ? kSgThreads / upr : 1;  // rows per block iteration
+  const int sub = upr <= kSgThreads ? t / upr : 0;
+  const int u0 = upr <= kSgThreads ? t - sub * upr : t;
+  if (sub >= R) return;                                    // idle half-warps (R * upr < 256)
+  const uint32_t hmask = 0xFFFFu << (t & 16);
+  const int64_t rstep = static_cast<int64_t>(gridDim.x) * R;
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * R; r0 < p.M; r0 += rstep) {
+    const int64_t row = r0 + sub;
+    if (row >= p.M) break;                                 // uniform per half-warp
+    const uint16_t* hrow = p.h + row * p.ldh;
+    for (int u = u0; u < upr; u += kSgThreads) {           // uniform per half-warp
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(hrow + u * 8));
+      const uint4 up = __ldg(reinterpret_cast<const uint4*>(hrow + p.I + u * 8));
+      uint4 v;
+      v.x = swiglu_pair(g.x, up.x);
+      v.y = swiglu_pair(g.y, up.y);
+      v.z = swiglu_pair(g.z, up.z);
+      v.w = swiglu_pair(g.w, up.w);
+      uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
 #pragma unroll
-    for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));  // the 16 lanes of a group
-    const Divisor d = group_divisor(tab, m, p.pow2 != 0);
-    if (u < p.units) {
-      const int64_t row = u / upr, c = u - row * upr;
-      *reinterpret_cast<uint2*>(p.q + row * p.I + c * 8) = quant8m(v, d);
-      if ((c & 15) == 0) p.s[(c >> 4) * p.M + row] = d.s;
+      for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(hmask, m, o));  // the 16 lanes of a group
+      const Divisor d = group_divisor(tab, m, p.pow2 != 0);
+      *reinterpret_cast<uint2*>(p.q + row * p.I + u * 8) = quant8m(v, d);
+      if ((u & 15) == 0) p.s[static_cast<int64_t>(u >> 4) * p.M + row] = d.s;
     }
   }
 }
@@ -883,7 +891,9 @@ cudaError_t launch_swiglu_quantize(const uint16_t* h, int64_t M, int64_t I, int6
     if (e != cudaSuccess) return e;
     per_sm = n > 0 ? n : 1;
   }
-  const int64_t need = (p.units + kSgThreads - 1) / kSgThreads;
+  const int64_t upr = I / 8;
+  const int64_t rows_per_block = upr <= kSgThreads ? kSgThreads / upr : 1;
+  const int64_t need = (M + rows_per_block - 1) / rows_per_block;
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   swiglu_quant_kernel<<<static_cast<int>(need < slots ? need : slots), kSgThreads, 0, stream>>>(p);
   return cudaGetLastError();
