@@ -801,24 +801,41 @@ __global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluPa
   if (sub >= R) return;                                    // idle half-warps (R * upr < 256)
   const uint32_t hmask = 0xFFFFu << (t & 16);
   const int64_t rstep = static_cast<int64_t>(gridDim.x) * R;
-  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * R; r0 < p.M; r0 += rstep) {
-    const int64_t row = r0 + sub;
-    if (row >= p.M) break;                                 // uniform per half-warp
-    const uint16_t* hrow = p.h + row * p.ldh;
-    for (int u = u0; u < upr; u += kSgThreads) {           // uniform per half-warp
-      const uint4 g = __ldg(reinterpret_cast<const uint4*>(hrow + u * 8));
-      const uint4 up = __ldg(reinterpret_cast<const uint4*>(hrow + p.I + u * 8));
-      uint4 v;
-      v.x = swiglu_pair(g.x, up.x);
-      v.y = swiglu_pair(g.y, up.y);
-      v.z = swiglu_pair(g.z, up.z);
-      v.w = swiglu_pair(g.w, up.w);
-      uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
+  auto process = [&](int64_t row, int u, const uint4& g, const uint4& up) {
+    uint4 v;
+    v.x = swiglu_pair(g.x, up.x);
+    v.y = swiglu_pair(g.y, up.y);
+    v.z = swiglu_pair(g.z, up.z);
+    v.w = swiglu_pair(g.w, up.w);
+    uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
 #pragma unroll
-      for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(hmask, m, o));  // the 16 lanes of a group
-      const Divisor d = group_divisor(tab, m, p.pow2 != 0);
-      *reinterpret_cast<uint2*>(p.q + row * p.I + u * 8) = quant8m(v, d);
-      if ((u & 15) == 0) p.s[static_cast<int64_t>(u >> 4) * p.M + row] = d.s;
+    for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(hmask, m, o));  // the 16 lanes of a group
+    const Divisor d = group_divisor(tab, m, p.pow2 != 0);
+    *reinterpret_cast<uint2*>(p.q + row * p.I + u * 8) = quant8m(v, d);
+    if ((u & 15) == 0) p.s[static_cast<int64_t>(u >> 4) * p.M + row] = d.s;
+  };
+  auto load = [&](int64_t row, int u, uint4& g, uint4& up) {
+    const uint16_t* hrow = p.h + row * p.ldh + u * 8;
+    g = __ldg(reinterpret_cast<const uint4*>(hrow));
+    up = __ldg(reinterpret_cast<const uint4*>(hrow + p.I));
+  };
+  if (upr <= kSgThreads) {
+    // one unit per row: the next row's loads are issued before this row is processed
+    int64_t row = static_cast<int64_t>(blockIdx.x) * R + sub;
+    uint4 ng = make_uint4(0u, 0u, 0u, 0u), nu = ng;
+    if (row < p.M) load(row, u0, ng, nu);
+    for (; row < p.M; row += rstep) {                      // uniform per half-warp
+      const uint4 g = ng, up = nu;
+      if (row + rstep < p.M) load(row + rstep, u0, ng, nu);
+      process(row, u0, g, up);
+    }
+  } else {
+    for (int64_t row = blockIdx.x; row < p.M; row += rstep) {
+      for (int u = u0; u < upr; u += kSgThreads) {         // uniform per half-warp
+        uint4 g, up;
+        load(row, u, g, up);
+        process(row, u, g, up);
+      }
     }
   }
 }

@@ -71,7 +71,7 @@ def _run(h_bits, inter, pow2):
     return to_host(q), to_host(s).T.copy()
 
 
-@pytest.mark.parametrize("M,I", [(128, 128), (3, 256), (257, 2048), (1024, 2048)])
+@pytest.mark.parametrize("M,I", [(128, 128), (3, 256), (257, 2048), (1024, 2048), (65, 4096)])
 @pytest.mark.parametrize("pow2", [False, True])
 def test_swiglu_quantize(M, I, pow2):
     h = synth.normal_bf16((M, 2 * I), 1.7, 50 + M, 5)
