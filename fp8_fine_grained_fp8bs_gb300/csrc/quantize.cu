@@ -323,7 +323,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileParams p) {
   using Q = QCfg<kMode>;
   extern __shared__ uint8_t qsmem_raw[];
-  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, offset from the shared array itself so that the
+  // compiler keeps the shared address space (shared loads and stores rather
+  // than generic ones)
+  uint8_t* tiles = qsmem_raw + ((1024u - (smem_u32(qsmem_raw) & 1023u)) & 1023u);
   // transposed codes of the current tile (block layouts): row R of the
   // tile's X^T part as 16 units of 8 codes, unit u stored at u ^ (R / 8)
   uint2 (*stg)[kGroup / 8] = reinterpret_cast<uint2 (*)[kGroup / 8]>(tiles + Q::kStages * kTileBytes);
