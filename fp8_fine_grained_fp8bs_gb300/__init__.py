@@ -23,7 +23,7 @@ __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
     "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
-    "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string",
+    "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string", "fp8bs_selftest_wait_timeout",
     "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1", "swiglu_quantize",
     "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128", "SCALE_ABSMAX", "SCALE_POW2",
 ]
@@ -58,6 +58,7 @@ _SIGNATURES = {
     "fp8bs_grouped_gemm": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                            _c_vp],
     "fp8bs_get_device_status": [_c_vp],
+    "fp8bs_selftest_wait_timeout": [_c_i64, _c_vp],
     "fp8bs_set_wait_timeout_ms": [_c_i64],
     "fp8bs_status_string": [_c_int],
 }
@@ -159,6 +160,10 @@ def fp8bs_grouped_gemm(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N
 
 def fp8bs_get_device_status(stream=None) -> int:
     return load_library().fp8bs_get_device_status(_stream(stream))
+
+
+def fp8bs_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(load_library().fp8bs_selftest_wait_timeout(int(timeout_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
 
 
 def fp8bs_set_wait_timeout_ms(ms: int):

@@ -191,6 +191,15 @@ int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const
   return run_gemm(g, stream);
 }
 
+int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return FP8BS_ERR_INVALID_ARG;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_wait_timeout_selftest(static_cast<uint64_t>(timeout_us) * 1000ull,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
   int v = 0, q = 0;

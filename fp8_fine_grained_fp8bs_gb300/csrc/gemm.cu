@@ -659,6 +659,23 @@ cudaError_t launch_gemm(const GemmArgs& a, int sm_count, cudaStream_t stream, bo
                 : run<256, false, false, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
 }
 
+// Diagnostic kernel: one thread waits, through the same bounded mbarrier
+// wait every kernel here uses, on a barrier that nothing arrives on; when the
+// wait gives up it records FP8BS_ERR_TIMEOUT in the GEMM status word and the
+// kernel returns normally.  No copies or MMAs are in flight.
+__global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait(&bar, 0, timeout_ns)) record_status(kStatusTimeout);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_take_status(int* status) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int));

@@ -60,4 +60,8 @@ cudaError_t launch_gemm(const GemmArgs& args, int sm_count, cudaStream_t stream,
 // copy on the current device.
 cudaError_t gemm_take_status(int* status);
 
+// Diagnostic: a kernel whose bounded wait runs out (nothing ever arrives on
+// its barrier) and records FP8BS_ERR_TIMEOUT in the GEMM status word.
+cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, cudaStream_t stream);
+
 }  // namespace fp8bs

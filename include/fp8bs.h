@@ -220,6 +220,14 @@ int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total,
  */
 int fp8bs_get_device_status(void* stream);
 
+/* Diagnostic of the failure path: launches a kernel that waits, through the
+ * same bounded mbarrier wait every kernel here uses, on a barrier nothing
+ * arrives on.  After `timeout_us` microseconds (1 .. 10^7) the wait gives up,
+ * the kernel records FP8BS_ERR_TIMEOUT and returns normally, so the next
+ * fp8bs_get_device_status() reports FP8BS_ERR_TIMEOUT and the CUDA context
+ * stays usable.  Returns FP8BS_OK once the kernel is launched. */
+int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream);
+
 /* Sets the limit of every bounded device wait, in milliseconds (default
  * 2000; 0 restores the default).  Applies to launches made after the call. */
 int fp8bs_set_wait_timeout_ms(int64_t ms);

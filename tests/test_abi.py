@@ -117,6 +117,11 @@ def test_grouped_gemm_argument_errors(lib):
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
 
 
+def test_selftest_argument_errors(lib):
+    assert lib.fp8bs_selftest_wait_timeout(0, None) == 1
+    assert lib.fp8bs_selftest_wait_timeout(20000000, None) == 1
+
+
 def test_timeout_setting(lib):
     assert lib.fp8bs_set_wait_timeout_ms(-1) == 1
     assert lib.fp8bs_set_wait_timeout_ms(500) == 0

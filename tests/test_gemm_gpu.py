@@ -183,3 +183,17 @@ def test_bad_arguments_raise():
     with pytest.raises(fp8bs.Fp8bsError) as e:
         fp8bs.fp8bs_gemm(a, s, a, s, 0, s, 0, 128, 128, 200)
     assert e.value.status == 2
+
+
+def test_bounded_wait_expires_and_context_stays_usable():
+    """A wait that nothing completes gives up after its limit, the status word
+    reports FP8BS_ERR_TIMEOUT (read once, then cleared), and a GEMM launched
+    afterwards runs correctly."""
+    torch, fp8bs = require_gpu()
+    assert fp8bs.fp8bs_get_device_status() == 0
+    fp8bs.fp8bs_selftest_wait_timeout(20000)          # 20 ms
+    assert fp8bs.fp8bs_get_device_status() == 6       # FP8BS_ERR_TIMEOUT
+    assert fp8bs.fp8bs_get_device_status() == 0       # cleared by the read
+    x, w = synth.tiny_fprop(0)
+    _fprop(x, w, out_bf16=False)
+    assert fp8bs.fp8bs_get_device_status() == 0
