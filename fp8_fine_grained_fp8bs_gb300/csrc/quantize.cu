@@ -9,6 +9,11 @@
 // reciprocal by Markstein's fused multiply-add correction (quant_pair
 // below), so every byte is read once and written once and no element needs
 // a division.
+//
+// Also here: the power-of-two scale mode (§3.3.3 "low-precision
+// activations" (1)), the FP8 re-tiling 1x128 -> 128x1 of the backward pass
+// (§3.5.2 "support for transposed GEMM operations"), and the fused SwiGLU ->
+// 1x128 quantisation of the MoE down projection's input (§3.3.3 (2)).
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
