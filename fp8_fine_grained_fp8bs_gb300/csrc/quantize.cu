@@ -674,8 +674,8 @@ __device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
 }
 
 __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantParams p) {
-  __shared__ uint32_t colred[kRqThreads / 32][kGroup];  // per-warp column maxima (|v| bits)
-  __shared__ float colmax[kGroup];
+  __shared__ float colred[kRqThreads / 32][kGroup];     // per-warp column maxima of |v|
+  __shared__ float2 coldiv[kGroup];                     // per column: (s, RN(1/s)), fast path flag in the sign of y
   // Output tile: row R of X^T's tile (tile column R) as 16 units of 8 codes;
   // unit u of row R is stored at u ^ (R / 8), so the 8-byte writes of a warp
   // (16 rows R = 8c+i, one unit each) hit 16 different bank pairs.
@@ -717,14 +717,14 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
     load(tile + gridDim.x, nq, ns);  // the next tile's codes and scales are in flight meanwhile
     const int64_t rb = tile / p.nkb;
     const int kb = static_cast<int>(tile - rb * p.nkb);
-    // column maxima of |v| (non-negative floats order like their bits)
-    uint32_t m[8];
+    // column maxima of |v|
+    float m[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      uint32_t a = 0;
+      float a = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) a = max(a, __float_as_uint(v[i][j]) & 0x7FFFFFFFu);
-      m[i] = max(a, __shfl_xor_sync(0xffffffffu, a, 16));  // the other row group of this warp
+      for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[i][j]));
+      m[i] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));  // the other row group of this warp
     }
     if (lane < 16) {
 #pragma unroll
@@ -732,17 +732,22 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
     }
     __syncthreads();
     if (t < kGroup) {
-      uint32_t a = colred[0][t];
+      // one divisor per column, shared with the 16 threads that quantise it
+      float amax = colred[0][t];
 #pragma unroll
-      for (int w = 1; w < kRqThreads / 32; ++w) a = max(a, colred[w][t]);
-      const float amax = __uint_as_float(a);
-      colmax[t] = amax;
-      p.sx_t[rb * p.K + static_cast<int64_t>(kb) * kGroup + t] = divisor_f32(amax, p.pow2 != 0).s;
+      for (int w = 1; w < kRqThreads / 32; ++w) amax = fmaxf(amax, colred[w][t]);
+      const Divisor d = divisor_f32(amax, p.pow2 != 0);
+      coldiv[t] = make_float2(d.s, d.fast ? d.y : -1.0f);
+      p.sx_t[rb * p.K + static_cast<int64_t>(kb) * kGroup + t] = d.s;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const Divisor d = divisor_f32(colmax[8 * c + i], p.pow2 != 0);
+      const float2 sd = coldiv[8 * c + i];
+      Divisor d;
+      d.s = sd.x;
+      d.fast = sd.y > 0.0f;
+      d.y = sd.y;
       stg[8 * c + i][g ^ c] = quant8f(v[i], d);
     }
     __syncthreads();
