@@ -275,7 +275,8 @@ struct QShared {
   DivTable tab;
   uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
   uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
-  uint32_t colmax[kGroup / 2];                         // dual: column maxima of the tile, two per word
+  float2 rowdiv[kGroup];                               // dual: per row (s, RN(1/s)); y < 0: exact path
+  float2 coldiv[kGroup];                               // dual: per column, the same
 };
 
 template <int kMode>
@@ -514,12 +515,16 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 #pragma unroll
         for (int o = 1; o <= 8; o <<= 1) am[i] = umax16x2(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
       }
+      // one divisor per row, computed by one thread of the row's half-warp
+      // and shared through shared memory with the other fifteen
+      if (c < 8) {
+        uint32_t a16 = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
+        for (int j = 0; j < 8; ++j)
+          if (j == c) a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
         const Divisor d = group_divisor(S.tab, a16, p.pow2 != 0);
-        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = quant8m(v[j], d);
-        if (c == 0) p.s[static_cast<int64_t>(kb) * p.rows + r0 + j] = d.s;
+        S.rowdiv[8 * g + c] = make_float2(d.s, d.fast ? d.y : -1.0f);
+        p.s[static_cast<int64_t>(kb) * p.rows + r0 + c] = d.s;
       }
       // 128x1 groups: transpose the 8x8 sub-block (column i of the tile
       // chunk becomes vector i: rows 8g .. 8g+7 of that column), reduce the
@@ -549,22 +554,27 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
         break;
       }
-      if (t < kGroup / 2) {
-        uint32_t m = S.colred[0][t];
+      if (t < kGroup) {  // one divisor per column
+        uint32_t m = S.colred[0][t >> 1];
 #pragma unroll
-        for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t]);
-        S.colmax[t] = m;
-        float* st = p.s_t + rb * K + static_cast<int64_t>(kb) * kGroup + 2 * t;
-        st[0] = group_divisor(S.tab, m & 0xFFFFu, p.pow2 != 0).s;
-        st[1] = group_divisor(S.tab, m >> 16, p.pow2 != 0).s;
+        for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t >> 1]);
+        const Divisor d = group_divisor(S.tab, (t & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
+        S.coldiv[t] = make_float2(d.s, d.fast ? d.y : -1.0f);
+        p.s_t[rb * K + static_cast<int64_t>(kb) * kGroup + t] = d.s;
       }
       compute_bar();
+      auto shared_divisor = [](float2 sd) {
+        Divisor d;
+        d.s = sd.x;
+        d.y = sd.y;
+        d.fast = sd.y > 0.0f;
+        return d;
+      };
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t m = S.colmax[4 * c + (i >> 1)];
-        const Divisor d = group_divisor(S.tab, (i & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
-        stg[8 * c + i][g ^ c] = quant8m(vt[i], d);
-      }
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = quant8m(v[j], shared_divisor(S.rowdiv[8 * g + j]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) stg[8 * c + i][g ^ c] = quant8m(vt[i], shared_divisor(S.coldiv[8 * c + i]));
     }
     // write the staged transposed codes: 8 threads per 128-byte row
     compute_bar();
