@@ -118,3 +118,23 @@ def test_moe_full_workload_sampled():
             check_bf16(got, Y, T, f"moe expert {g}")
         pad = torch.as_tensor(np.nonzero(src < 0)[0], device=y.device)
         assert int(torch.count_nonzero(y[pad])) == 0
+
+
+def test_grouped_with_power_of_two_activation_scales():
+    """The activations dispatched before the MoE up projection carry
+    power-of-two scales (§3.3.3 "low-precision communication"); the grouped
+    GEMM consumes them like any other float32 scale."""
+    torch, fp8bs = require_gpu()
+    G, N, K = 3, 256, 512
+    offsets = np.array([0, 256, 384, 640], np.int64)
+    x = synth.normal_bf16((640, K), 1.0, 9, 1, outliers=True)
+    w = synth.normal_bf16((G, N, K), 0.02, 9, 5)
+    xq, sx = fp8bs.quantize_act(to_dev_bf16(x), pow2=True)
+    wq, sw = _quantize_weights(fp8bs, w)
+    y = to_host(fp8bs.grouped_gemm(xq, sx, to_dev(offsets.astype(np.int32)), wq, sw, out_dtype=torch.float32))
+    assert fp8bs.fp8bs_get_device_status() == 0
+    qa, sa = oracle.quantize_act_1x128(x, pow2=True)
+    qb = np.stack([oracle.quantize_weight_128x128(w[g])[0] for g in range(G)])
+    sb = np.stack([oracle.quantize_weight_128x128(w[g])[1] for g in range(G)])
+    Y, T = oracle.grouped_gemm_block_scaled(qa, sa, offsets, qb, sb)
+    check_f32(y, Y, T, "grouped, power-of-two activation scales")
