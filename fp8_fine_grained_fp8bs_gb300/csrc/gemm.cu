@@ -624,14 +624,12 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
   cfg.stream = stream;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  static int max_clusters = 0;  // co-resident clusters of this configuration
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
-    int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (err != cudaSuccess) return err;
-    max_clusters = n > 0 ? n : 1;
-  }
+  static std::atomic<int> cluster_cache[kMaxCachedDevices];  // co-resident clusters, per device
+  int max_clusters = 0;
+  cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+  err = cached_per_device(cluster_cache, [&](int* n) { return cudaOccupancyMaxActiveClusters(n, kern, &cfg); },
+                          &max_clusters);
+  if (err != cudaSuccess) return err;
   cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
   err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, kp);
   if (err != cudaSuccess) return err;

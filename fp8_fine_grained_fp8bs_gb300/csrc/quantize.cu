@@ -618,13 +618,12 @@ cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int
   constexpr int smem = q_smem_bytes<kMode>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  static int per_sm = 0;  // co-resident CTAs per SM
-  if (per_sm == 0) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kQThreads, smem);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
+  static std::atomic<int> per_sm_cache[kMaxCachedDevices];  // co-resident CTAs per SM, per device
+  int per_sm = 0;
+  e = cached_per_device(
+      per_sm_cache, [&](int* n) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, kQThreads, smem); },
+      &per_sm);
+  if (e != cudaSuccess) return e;
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   const int grid = static_cast<int>(ntiles < slots ? ntiles : slots);
   kern<<<grid, kQThreads, smem, stream>>>(map, p);
@@ -900,13 +899,12 @@ cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, in
   p.sx_t = sx_t;
   p.pow2 = pow2 ? 1 : 0;
   if (p.ntiles <= 0) return cudaSuccess;
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, requant_kernel, kRqThreads, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
+  static std::atomic<int> per_sm_cache[kMaxCachedDevices];
+  int per_sm = 0;
+  const cudaError_t e = cached_per_device(
+      per_sm_cache, [](int* n) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, requant_kernel, kRqThreads, 0); },
+      &per_sm);
+  if (e != cudaSuccess) return e;
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   requant_kernel<<<static_cast<int>(p.ntiles < slots ? p.ntiles : slots), kRqThreads, 0, stream>>>(p);
   return cudaGetLastError();
@@ -924,13 +922,13 @@ cudaError_t launch_swiglu_quantize(const uint16_t* h, int64_t M, int64_t I, int6
   p.units = M * (I / 8);
   p.pow2 = pow2 ? 1 : 0;
   if (p.units <= 0) return cudaSuccess;
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_quant_kernel, kSgThreads, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
+  static std::atomic<int> per_sm_cache[kMaxCachedDevices];
+  int per_sm = 0;
+  const cudaError_t e = cached_per_device(
+      per_sm_cache,
+      [](int* n) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, swiglu_quant_kernel, kSgThreads, 0); },
+      &per_sm);
+  if (e != cudaSuccess) return e;
   const int64_t upr = I / 8;
   const int64_t rows_per_block = upr <= kSgThreads ? kSgThreads / upr : 1;
   const int64_t need = (M + rows_per_block - 1) / rows_per_block;
