@@ -67,8 +67,8 @@ def _peaks():
 
 
 def _traffic(kernel_key: str, source_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    source still matches the one the counters were taken on."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary, if
+    the kernel source still matches the one the counters were taken on."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -79,7 +79,7 @@ def _traffic(kernel_key: str, source_file: str):
         return None
     with open(os.path.join(ROOT, source_file), "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return e["bytes_per_launch"] if e.get("source_sha256_16") == h else None
+    return e["dram_bytes_per_launch"] if e.get("source_sha256_16") == h else None
 
 
 class ClockSampler:

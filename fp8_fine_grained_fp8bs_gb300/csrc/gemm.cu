@@ -58,34 +58,63 @@ constexpr int kScaleChunk = 8;
 constexpr int kScaleChunks = 2;
 constexpr int kScaleSlots = kScaleChunk * kScaleChunks;
 constexpr uint32_t kTmemCols = 512;  // all of TMEM: 512 / BN partial buffers
-constexpr uint32_t kRegsProducer = 56;
-constexpr uint32_t kRegsEpilogue = 224;
+// Register split (setmaxnreg): the four producer/issuer warps shrink to
+// kRegsProducer, the eight epilogue warps grow to kRegsEpilogue, which holds
+// the 128 FP32 accumulators, two 32-column TMEM reads in flight and the
+// loop state without spilling; 4 x 32 x 40 + 8 x 32 x 232 = 384 x 168, the
+// CTA's allocation at launch.
+constexpr uint32_t kRegsProducer = 40;
+constexpr uint32_t kRegsEpilogue = 232;
+
+// Output staging: each epilogue warp writes its 32 rows x BN/2 columns
+// through kOutSlots boxes of 32 rows x 128 bytes in shared memory (128-byte
+// swizzled, the layout TMA expects), each stored by one TMA copy.
+constexpr int kOutRows = 32;
+constexpr int kOutBoxBytes = kOutRows * 128;
+constexpr int kOutSlots = 2;
+constexpr int kSmemBudget = 227 * 1024;
 
 // BN is the tile width of one CTA's output; with kPair (2-SM MMA) each CTA
 // holds only half of the B tile's rows in its shared memory.
-template <int BN, bool kPair>
+template <int BN, bool kPair, bool kRowScale>
 struct Cfg {
   static constexpr int kABytes = kBlockM * kBlockK;                   // 16 KB
   static constexpr int kBBytes = (kPair ? BN / 2 : BN) * kBlockK;     // 16 or 32 KB per CTA
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kStageBytes >= 48 * 1024 ? 4 : kStageBytes >= 32 * 1024 ? 6 : 8;
   // TMEM partial buffers: the MMA of k-block j+kBufs may start only once
   // the epilogue has read k-block j out, so more buffers hide more of that
   // hand-off (commit, TMEM read-out, release) behind tensor-core work.
   static constexpr int kBufs = static_cast<int>(kTmemCols) / BN;
-  static constexpr int kSlotFloats = kBlockM + BN;        // A row scales, then B column scales
+  // scale slot: A row scales, then B scales (per column, or one per
+  // 128-column block padded to 16 bytes)
+  static constexpr int kSlotFloats = kBlockM + (kRowScale ? BN : 4);
   static constexpr int kColsPerThread = BN / 2;
   static constexpr int kChunks = kColsPerThread / 32;
+  static constexpr int kOutBytes = (kEpiThreads / 32) * kOutSlots * kOutBoxBytes;
+  static constexpr int kMaxStages = 6;
+  static constexpr int kNumBarsMax = 2 * kMaxStages + 2 * kScaleChunks + 2 * kBufs + 2;
+  static constexpr int kFixedBytes =
+      kOutBytes + kScaleSlots * kSlotFloats * 4 + kNumBarsMax * 8 + 16 + 2 * (kMaxGroups + 1) * 4 + 1024;
+  // Operand ring: as many stages as the rest leaves room for, rounded down
+  // to an even count.  The two MMA-issuing warps take alternate k-block
+  // steps, so with an even ring each stage is only ever consumed by the
+  // same warp, which therefore never waits on a stage more than one phase
+  // ahead of its barrier.
+  static constexpr int kFit = (kSmemBudget - kFixedBytes) / kStageBytes;
+  static constexpr int kStages = (kFit < kMaxStages ? kFit : kMaxStages) & ~1;
+  static_assert(kStages >= 4, "operand ring too shallow");
   // dynamic shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
-  static constexpr int kOffScale = kOffB + kStages * kBBytes;
+  static constexpr int kOffOut = kOffB + kStages * kBBytes;             // 1024-aligned
+  static constexpr int kOffScale = kOffOut + kOutBytes;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
   static constexpr int kNumBars = 2 * kStages + 2 * kScaleChunks + 2 * kBufs + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;       // tmem slot, abort flag, tile count
   static constexpr int kOffGroups = kOffMisc + 16;              // offsets[G+1], cum[G+1]
   static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kOffOut % 1024 == 0, "staging boxes need 1024-byte alignment for the 128-byte swizzle");
+  static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
 };
 
 struct KParams {
@@ -127,6 +156,52 @@ __device__ __forceinline__ void fold_row(float2* acc, const uint32_t (&p)[32], f
   }
 }
 
+// Stores one thread's row segment, kCols FP32 accumulators starting at
+// column x0 of row y0 + lane, for the 32 rows of its warp: per 128-byte
+// column block the warp writes its rows into a staging box (16-byte chunk c
+// of row r at chunk position c ^ (r % 8), the 128-byte swizzle), and lane 0
+// stores the box with TMA (or adds it into D).  Boxes rotate over kOutSlots
+// staging slots; a slot is rewritten only once the store that last used it
+// has read it out.  `seq` counts the warp's boxes over the kernel (one bulk
+// group each).
+template <int kCols, bool kBf16>
+__device__ __forceinline__ void store_segment(const float* acc, uint8_t* slots, uint32_t& seq, int lane,
+                                              const CUtensorMap* tmD, int x0, int y0, bool add) {
+  constexpr int kPerChunk = kBf16 ? 8 : 4;   // columns in 16 bytes
+  constexpr int kBoxCols = 8 * kPerChunk;    // columns in 128 bytes
+  static_assert(kCols % kBoxCols == 0, "segment of whole boxes");
+#pragma unroll
+  for (int b = 0; b < kCols / kBoxCols; ++b, ++seq) {
+    uint8_t* box = slots + (seq % kOutSlots) * kOutBoxBytes;
+    if (lane == 0) bulk_wait_read<kOutSlots - 1>();
+    __syncwarp();
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float* v = acc + b * kBoxCols + c * kPerChunk;
+      uint4 w;
+      if (kBf16) {
+        w.x = pack_bf16x2(v[0], v[1]);
+        w.y = pack_bf16x2(v[2], v[3]);
+        w.z = pack_bf16x2(v[4], v[5]);
+        w.w = pack_bf16x2(v[6], v[7]);
+      } else {
+        w = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+      }
+      *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = w;
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      if (add)
+        tma_reduce_add_2d(tmD, box, x0 + b * kBoxCols, y0);
+      else
+        tma_store_2d(tmD, box, x0 + b * kBoxCols, y0);
+      bulk_commit();
+    }
+  }
+}
+
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_status, 0, code); }
 
 // A bounded mbarrier wait made by a whole warp, with lane 0's outcome.  The
@@ -138,13 +213,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __shfl_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns), 0);
 }
 
-// Tile t -> (first row, first column, group).  Tiles run m-tile-major with
-// the BN-wide n-tiles of one m-tile consecutive, so concurrently running
-// CTAs share A rows.
+// Work unit t -> (first row, first column, group, end of the rows the
+// unit may write).  Units run m-tile-major with the BN-wide n-tiles of one
+// m-tile consecutive, so concurrently running CTAs share A rows.
 //
 // With CTA pairs (a cluster of two running one 2-SM MMA over a 256-row
-// tile), work unit t names an (m-tile pair, n-tile); the CTA of rank r
-// takes m-tile 2*(pair) + r.
+// tile), unit t names an (m-tile pair, n-tile) and the CTA of rank r takes
+// the pair's m-tile r.  In the grouped GEMM the pairs are formed within
+// each group's segment (s_cum counts units per group); a group with an odd
+// number of m-tiles ends in a pair whose second m-tile lies past the
+// segment: that CTA still loads its half of B and joins the MMA, and stores
+// nothing (row0 >= row_end).
 //
 // Every role walks the k-blocks of work unit t starting at t % (K/128) and
 // wrapping around: CTAs that share an A or B tile then read different
@@ -153,28 +232,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 // order).
 template <int BN, bool kPair>
 __device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const int* s_off, const int* s_cum,
-                                            int num_groups, uint32_t rank, int& row0, int& n0, int& g) {
-  const int mu = t / ntn;
-  const int mt = kPair ? 2 * mu + static_cast<int>(rank) : mu;
+                                            int num_groups, uint32_t rank, int64_t M, int& row0, int& n0, int& g,
+                                            int64_t& row_end) {
+  const int mu = t / ntn;  // m-tile, or m-tile pair
   n0 = (t - mu * ntn) * BN;
   if (!grouped) {
     g = 0;
-    row0 = mt * kBlockM;
+    row0 = (kPair ? 2 * mu + static_cast<int>(rank) : mu) * kBlockM;
+    row_end = M;
     return;
   }
-  int lo = 0, hi = num_groups - 1;  // last g with cum[g] <= mt
+  int lo = 0, hi = num_groups - 1;  // last g with cum[g] <= mu
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_cum[mid] <= mt) lo = mid; else hi = mid - 1;
+    if (s_cum[mid] <= mu) lo = mid; else hi = mid - 1;
   }
   g = lo;
-  row0 = s_off[g] + (mt - s_cum[g]) * kBlockM;
+  const int local = kPair ? 2 * (mu - s_cum[g]) + static_cast<int>(rank) : mu - s_cum[g];
+  row0 = s_off[g] + local * kBlockM;
+  row_end = s_off[g + 1];
 }
 
 template <int BN, bool kRowScale, bool kGrouped, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using C = Cfg<BN, kPair>;
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmD, const KParams p) {
+  using C = Cfg<BN, kPair, kRowScale>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem + C::kOffA;
@@ -229,9 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prev = o;
       }
       if (ok) {
-        for (int g = 0; g < p.num_groups; ++g) {
+        for (int g = 0; g < p.num_groups; ++g) {  // work units (m-tiles or m-tile pairs) per group
           s_cum[g] = total_mt;
-          total_mt += (s_off[g + 1] - s_off[g]) / kBlockM;
+          const int mt = (s_off[g + 1] - s_off[g]) / kBlockM;
+          total_mt += kPair ? (mt + 1) / 2 : mt;
         }
         s_cum[p.num_groups] = total_mt;
       } else {
@@ -240,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       total_mt = static_cast<int>((p.M + kBlockM - 1) / kBlockM);
+      if (kPair) total_mt = (total_mt + 1) / 2;
     }
-    if (kPair) total_mt = (total_mt + 1) / 2;
     misc[1] = 0;  // abort flag
     misc[2] = static_cast<uint32_t>(total_mt * ntn);
   }
@@ -276,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
         int row0, n0, g;
-        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
+        int64_t row_end;
+        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
           if (!warp_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
           if (lane == 0) {
@@ -287,8 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (C::kABytes + C::kBBytes));
               const uint32_t leader_full = mapa_shared(&full[stage], 0);
               tma_load_2d_pair(sA + stage * C::kABytes, &tmA, leader_full, kb * kBlockK, row0);
-              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
-                               n0 + static_cast<int>(rank) * (BN / 2));
+              if (kGrouped)
+                tma_load_3d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
+                                 n0 + static_cast<int>(rank) * (BN / 2), g);
+              else
+                tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, leader_full, kb * kBlockK,
+                                 n0 + static_cast<int>(rank) * (BN / 2));
             } else {
               mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
               tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBlockK, row0);
@@ -382,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool live = true;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
         int row0, n0, g;
-        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
+        int64_t row_end;
+        tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         const bool last_tile = t + nunits >= total_tiles;
         for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, ++step, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
           const uint32_t chunk = (step / kScaleChunk) % kScaleChunks;
@@ -426,14 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
     const int colhalf = e >> 2;          // which BN/2 columns
     const int row_in_tile = quarter * 32 + lane;
+    uint8_t* s_out = smem + C::kOffOut + e * kOutSlots * kOutBoxBytes;
+    uint32_t out_seq = 0;
+    if (lane == 0 && e == 0) prefetch_tmap(&tmD);
     uint32_t buf = 0, tphase = 0;
     uint32_t step = 0;
     bool live = true;
     for (int t = unit0; t < total_tiles && live; t += nunits) {
       int row0, n0, g;
-      tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, row0, n0, g);
-      const int64_t m = static_cast<int64_t>(row0) + row_in_tile;
-      const bool mvalid = m < p.M;
+      int64_t row_end;
+      tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
       const int ncol0 = n0 + colhalf * C::kColsPerThread;
       const int bsel = (colhalf * C::kColsPerThread) / 128;   // which 128-column block of the tile
       float2 acc2[C::kColsPerThread / 2];
@@ -488,34 +580,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++buf == C::kBufs) { buf = 0; tphase ^= 1; }
       }
       if (!live) break;
-      // ---- store this thread's row segment
+      // ---- store the warp's 32 rows x BN/2 columns through shared memory
+      // and TMA; rows past M are clipped by the tensor map
       const float* acc = reinterpret_cast<const float*>(acc2);
-      if (mvalid && ncol0 < p.N) {
-        if (p.out_bf16) {
-          __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) + m * p.N + ncol0;
-#pragma unroll
-          for (int j = 0; j < C::kColsPerThread; j += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
-            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-            *reinterpret_cast<uint4*>(drow + j) = v;
-          }
-        } else {
-          float* drow = reinterpret_cast<float*>(p.d) + m * p.N + ncol0;
-#pragma unroll
-          for (int j = 0; j < C::kColsPerThread; j += 4) {
-            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-            if (p.accumulate) {
-              const float4 o = *reinterpret_cast<const float4*>(drow + j);
-              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-            }
-            *reinterpret_cast<float4*>(drow + j) = v;
-          }
-        }
+      const int y0 = row0 + quarter * 32;
+      if (y0 < row_end && ncol0 < p.N) {
+        if (p.out_bf16)
+          store_segment<C::kColsPerThread, true>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, false);
+        else
+          store_segment<C::kColsPerThread, false>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, p.accumulate != 0);
       }
     }
+    // the staging boxes stay in use until the last stores have completed
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!live) {
       record_status(kStatusTimeout);
       *abort_flag = 1;
@@ -554,9 +632,25 @@ bool encode_operand(CUtensorMap* map, const void* base, int rank, const uint64_t
   return r == CUDA_SUCCESS;
 }
 
+// Output D [rows][N] (BF16 or FP32, row-major) with a 128-byte x box_rows
+// box and 128-byte swizzling, for the epilogue's TMA stores.
+bool encode_output(CUtensorMap* map, void* base, int64_t rows, int64_t N, bool bf16, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const uint64_t elt = bf16 ? 2 : 4;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(N) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base,
+                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int BN, bool kRowScale, bool kGrouped, bool kPair>
 cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap_failed, bool* reg_check_failed) {
-  using C = Cfg<BN, kPair>;
+  using C = Cfg<BN, kPair, kRowScale>;
   auto kern = gemm_kernel<BN, kRowScale, kGrouped, kPair>;
   // The register split (warps 0-3 shrink to kRegsProducer, warps 4-11 grow
   // to kRegsEpilogue) must fit in what the CTA is launched with.
@@ -587,6 +681,9 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
     if (!encode_operand(&tmB, a.b, 2, dB, sB, b_rows)) { *tmap_failed = true; return cudaErrorInvalidValue; }
   }
 
+  CUtensorMap tmD;
+  if (!encode_output(&tmD, a.d, a.M, a.N, a.out_bf16, kOutRows)) { *tmap_failed = true; return cudaErrorInvalidValue; }
+
   KParams kp;
   kp.sa = a.sa;
   kp.sb = a.sb;
@@ -610,7 +707,7 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
   if (units <= 0) return cudaSuccess;
   if (!kPair) {
     const int grid = static_cast<int>(std::min<int64_t>(units, sm_count));
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, kp);
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, tmD, kp);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -631,7 +728,7 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
                           &max_clusters);
   if (err != cudaSuccess) return err;
   cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, kp);
+  err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, kp);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -645,10 +742,10 @@ cudaError_t launch_gemm(const GemmArgs& a, int sm_count, cudaStream_t stream, bo
   // 128-wide n-tiles when 256-wide ones would leave most SMs idle.
   const int64_t mt = (a.M + kBlockM - 1) / kBlockM;
   const bool narrow = a.N <= 128 || (!a.grouped && mt * ((a.N + 255) / 256) < sm_count);
-  if (a.grouped) {  // two m-tiles of a pair may belong to different experts: no pairs
+  if (a.grouped) {  // pairs formed within each expert's segment
     if (a.sb_row) return cudaErrorInvalidValue;
     return narrow ? run<128, false, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed)
-                  : run<256, false, true, false>(a, sm_count, stream, tmap_failed, reg_check_failed);
+                  : run<256, false, true, true>(a, sm_count, stream, tmap_failed, reg_check_failed);
   }
   if (a.sb_row)
     return narrow ? run<128, true, false, false>(a, sm_count, stream, tmap_failed, reg_check_failed)

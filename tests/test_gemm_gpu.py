@@ -65,6 +65,32 @@ def test_ragged_shapes_bf16(M, N, K):
     _fprop(x, w, out_bf16=True)
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16", "f32_accumulate"])
+def test_pair_tiles_ragged_rows(out):
+    """A shape that takes the 256x256 CTA-pair tiles (31 m-tiles x 5 n-tiles is
+    more work units than SMs): an odd number of m-tiles, so the last pair's
+    second tile lies wholly past M, and a partial last m-tile whose rows past
+    M the store clips; every element compared."""
+    torch, fp8bs = require_gpu()
+    M, N, K = 3900, 1280, 256
+    x = synth.normal_bf16((M, K), 1.0, 21, 1, outliers=True)
+    w = synth.normal_bf16((N, K), 0.02, 21, 2)
+    if out != "f32_accumulate":
+        _fprop(x, w, out_bf16=out == "bf16")
+        return
+    xq, sx = fp8bs.quantize_act(to_dev_bf16(x))
+    wq, sw = fp8bs.quantize_weight(to_dev_bf16(w))
+    d0 = np.random.default_rng(1).standard_normal((M, N)).astype(np.float32)
+    d = to_dev(d0)
+    fp8bs.gemm(xq, sx, wq, sw, out=d, accumulate=True)
+    assert fp8bs.fp8bs_get_device_status() == 0
+    qa, sa = oracle.quantize_act_1x128(x)
+    qb, sb = oracle.quantize_weight_128x128(w)
+    Y, T = oracle.gemm_block_scaled(qa, sa, qb, sb)
+    got = to_host(d).astype(np.float64)
+    assert np.all(np.abs(got - (d0 + Y)) <= 1e-5 * T + 2.0 ** -23 * np.abs(d0 + Y))
+
+
 def test_zero_and_padding_rows():
     x = synth.normal_bf16((256, 256), 1.0, 11, 1, outliers=True)
     x[5] = 0

@@ -60,23 +60,31 @@ def test_small_groups_full_compare(out_bf16):
     assert np.all(y[200:256] == 0) and np.all(y[500:] == 0)
 
 
-def test_rows_outside_groups_untouched():
+@pytest.mark.parametrize("N,offsets,rows", [
+    (128, [128, 256, 384], 512),         # 128-wide tiles: rows 0..127 and 384.. not in any group
+    (256, [128, 384, 512], 768),         # 256-wide tiles on CTA pairs: the second expert's one m-tile
+                                         # pairs with rows 512..639, which no group owns
+    (256, [0, 384, 384, 640], 768),      # three m-tiles, an empty expert, then two
+])
+def test_rows_outside_groups_untouched(N, offsets, rows):
     torch, fp8bs = require_gpu()
-    G, N, K = 2, 128, 256
-    offsets = np.array([128, 256, 384], np.int32)             # rows 0..127 and 384.. not in any group
-    x = synth.normal_bf16((512, K), 1.0, 3, 1)
+    offsets = np.array(offsets, np.int32)
+    G, K = len(offsets) - 1, 256
+    x = synth.normal_bf16((rows, K), 1.0, 3, 1)
     w = synth.normal_bf16((G, N, K), 0.02, 3, 5)
     xq, sx = fp8bs.quantize_act(to_dev_bf16(x))
     wq, sw = _quantize_weights(fp8bs, w)
-    out = torch.full((512, N), 7.0, dtype=torch.float32, device="cuda:0")
+    out = torch.full((rows, N), 7.0, dtype=torch.float32, device="cuda:0")
     fp8bs.grouped_gemm(xq, sx, to_dev(offsets), wq, sw, out=out)
+    assert fp8bs.fp8bs_get_device_status() == 0
     y = to_host(out)
-    assert np.all(y[:128] == 7.0) and np.all(y[384:] == 7.0)
+    lo, hi = int(offsets[0]), int(offsets[-1])
+    assert np.all(y[:lo] == 7.0) and np.all(y[hi:] == 7.0)
     qa, sa = oracle.quantize_act_1x128(x)
     qb = np.stack([oracle.quantize_weight_128x128(w[g])[0] for g in range(G)])
     sb = np.stack([oracle.quantize_weight_128x128(w[g])[1] for g in range(G)])
     Y, T = oracle.grouped_gemm_block_scaled(qa, sa, offsets, qb, sb)
-    check_f32(y[128:384], Y[128:384], T[128:384], "grouped offset segments")
+    check_f32(y[lo:hi], Y[lo:hi], T[lo:hi], "grouped offset segments")
 
 
 def test_invalid_offsets_reported():
