@@ -412,9 +412,16 @@ def main():
     sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
+    # The two quantisations are independent: W's runs on a second stream
+    # beside X's (both stream HBM; together they leave no half-empty last
+    # wave), and the GEMM waits for both.
+    s_w = torch.cuda.Stream(dev)
+
     def step(gemm_events=None):
+        s_w.wait_stream(stream)                     # the previous GEMM is done with wq
+        fp8bs.fp8bs_quantize_weight(win, N, K, K, wq, sw, None, None, s_w)
         fp8bs.fp8bs_quantize_act(xin, M, K, K, xq, sx, None, None, stream)
-        fp8bs.fp8bs_quantize_weight(win, N, K, K, wq, sw, None, None, stream)
+        stream.wait_stream(s_w)
         if gemm_events is not None:
             gemm_events[0].record(stream)
         fp8bs.fp8bs_gemm(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, y, fp8bs.OUT_BF16, M, N, K, 0, stream)

@@ -656,13 +656,22 @@ struct RequantParams {
 
 // Eight float32 values -> eight codes with one divisor (Markstein quotients
 // as quant_pair; IEEE divisions for a slow divisor; the sign bit of each
-// input ORed into its code to keep the sign of -0).
-__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d) {
+// input ORed into its code to keep the sign of -0).  With a power-of-two
+// divisor on the fast path y = 1/s is exact, so RN(x * y) already is the
+// correctly rounded quotient (and keeps the sign of -0): one multiply.
+__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d, bool pow2) {
   uint32_t c[4];
   if (!d.fast) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       c[j] = d.s == 0.0f ? 0u : e4m3x2(__fdiv_rn(v[2 * j], d.s), __fdiv_rn(v[2 * j + 1], d.s));
+  } else if (pow2) {
+    const float2 y2 = make_float2(d.y, d.y);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 q = __fmul2_rn(make_float2(v[2 * j], v[2 * j + 1]), y2);
+      c[j] = e4m3x2(q.x, q.y);
+    }
   } else {
     const float2 y2 = make_float2(d.y, d.y), ns2 = make_float2(-d.s, -d.s);
 #pragma unroll
@@ -757,7 +766,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
       d.s = sd.x;
       d.fast = sd.y > 0.0f;
       d.y = sd.y;
-      stg[8 * c + i][g ^ c] = quant8f(v[i], d);
+      stg[8 * c + i][g ^ c] = quant8f(v[i], d, p.pow2 != 0);
     }
     __syncthreads();
     // write the tile out: 8 threads per 128-byte row of X^T
