@@ -302,6 +302,35 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
     out["context_bf16_matmul"]["frac_of_bf16_peak"] = out["context_bf16_matmul"]["tflops"] / (fp8_peak / 2.0)
     del xa, wa, ya
 
+    # ---- context only: accumulation precision without promotion.  The pages
+    # (H800, all of K = 4096 accumulated in the tensor core) report a maximum
+    # relative error near 2%; the diagnostic GEMM accumulates all of K in
+    # tensor memory on this GPU, the production GEMM promotes every 128 K
+    # (block scales 1 here).  Reference: the float64 product of the decoded
+    # codes, exact for these sums (multiples of 2^-18 below 2^31).
+    Mc, Nc, Kc = 128, 256, 4096
+    ac = torch.randn((Mc, Kc), generator=g0, device=dev).to(torch.bfloat16)
+    bc = torch.randn((Nc, Kc), generator=g0, device=dev).to(torch.bfloat16)
+    acq, _ = fp8bs.quantize_act(ac, stream=stream)
+    bcq, _ = fp8bs.quantize_act(bc, stream=stream)
+    d_un = fp8bs.diag_gemm_unpromoted(acq, bcq, stream=stream)
+    d_pr = fp8bs.gemm(acq, torch.ones((Kc // 128, Mc), device=dev), bcq,
+                      torch.ones((Nc // 128, Kc // 128), device=dev), out_dtype=torch.float32, stream=stream)
+    torch.cuda.synchronize(dev)
+    yc = acq.view(torch.float8_e4m3fn).double() @ bcq.view(torch.float8_e4m3fn).double().t()
+    big = yc.abs() >= 0.1 * yc.pow(2).mean().sqrt()
+
+    def acc_err(d):
+        e = (d.double() - yc).abs()
+        return {"max_err_over_max_abs": float(e.max() / yc.abs().max()),
+                "max_rel_err": float((e[big] / yc[big].abs()).max())}
+
+    out["context_unpromoted_accumulation"] = {
+        "shape": f"{Mc}x{Nc}x{Kc}, E4M3 codes of N(0,1) in 1x128 groups, scales left out",
+        "unpromoted_tensor_core": acc_err(d_un), "promoted_every_128": acc_err(d_pr),
+        "pages_h800_unpromoted_max_rel_err": 0.02}
+    del ac, bc, acq, bcq, d_un, d_pr, yc, big
+
     # ---- weight quantize with the transposed copy
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + rank)

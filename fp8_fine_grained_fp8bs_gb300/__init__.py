@@ -24,6 +24,7 @@ __all__ = [
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
     "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string", "fp8bs_selftest_wait_timeout",
+    "fp8bs_diag_gemm_unpromoted", "diag_gemm_unpromoted",
     "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1", "swiglu_quantize",
     "OUT_F32", "OUT_BF16", "SCALE_BLOCK128x128", "SCALE_ROW1x128", "SCALE_ABSMAX", "SCALE_POW2",
 ]
@@ -59,6 +60,7 @@ _SIGNATURES = {
                            _c_vp],
     "fp8bs_get_device_status": [_c_vp],
     "fp8bs_selftest_wait_timeout": [_c_i64, _c_vp],
+    "fp8bs_diag_gemm_unpromoted": [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp],
     "fp8bs_set_wait_timeout_ms": [_c_i64],
     "fp8bs_status_string": [_c_int],
 }
@@ -166,6 +168,11 @@ def fp8bs_selftest_wait_timeout(timeout_us: int, stream=None):
     _check(load_library().fp8bs_selftest_wait_timeout(int(timeout_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
 
 
+def fp8bs_diag_gemm_unpromoted(a, b, d, M, N, K, stream=None):
+    _check(load_library().fp8bs_diag_gemm_unpromoted(_ptr(a), _ptr(b), _ptr(d), M, N, K, _stream(stream)),
+           "fp8bs_diag_gemm_unpromoted")
+
+
 def fp8bs_set_wait_timeout_ms(ms: int):
     _check(load_library().fp8bs_set_wait_timeout_ms(int(ms)), "fp8bs_set_wait_timeout_ms")
 
@@ -254,4 +261,15 @@ def grouped_gemm(a, sa, offsets, b, sb, out_dtype=None, out=None, stream=None):
         out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
     d_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     fp8bs_grouped_gemm(a, sa, M, offsets, G, b, sb, out, d_dtype, N, K, stream)
+    return out
+
+
+def diag_gemm_unpromoted(a, b, stream=None):
+    """Diagnostic: FP32 D = A B^T of E4M3 codes (A [M,K], B [N,K] uint8) with all
+    of K accumulated by the tensor core alone, no promotion and no scales."""
+    import torch
+    M, K = a.shape
+    N = b.shape[0]
+    out = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    fp8bs_diag_gemm_unpromoted(a, b, out, M, N, K, stream)
     return out

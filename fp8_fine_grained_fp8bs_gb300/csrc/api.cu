@@ -200,12 +200,29 @@ int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream) {
                                                        static_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_diag_gemm_unpromoted(const uint8_t* a, const uint8_t* b, float* d, int64_t M, int64_t N, int64_t K,
+                               void* stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M % 128 != 0 || N % 256 != 0 || K % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (K == 0) return FP8BS_ERR_SHAPE;
+  if (a == nullptr || b == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_unpromoted_gemm(a, b, d, M, N, K, g_timeout_ns.load(),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-  int v = 0, q = 0;
+  int v = 0, q = 0, dg = 0;
   if (fp8bs::gemm_take_status(&v) != cudaSuccess) return FP8BS_ERR_CUDA;
   if (fp8bs::quant_take_status(&q) != cudaSuccess) return FP8BS_ERR_CUDA;
-  return v != FP8BS_OK ? v : q;
+  if (fp8bs::diag_take_status(&dg) != cudaSuccess) return FP8BS_ERR_CUDA;
+  return v != FP8BS_OK ? v : q != FP8BS_OK ? q : dg;
 }
 
 int fp8bs_set_wait_timeout_ms(int64_t ms) {

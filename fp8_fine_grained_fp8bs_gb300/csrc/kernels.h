@@ -64,4 +64,13 @@ cudaError_t gemm_take_status(int* status);
 // its barrier) and records FP8BS_ERR_TIMEOUT in the GEMM status word.
 cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, cudaStream_t stream);
 
+// Diagnostic GEMM without promotion (diag.cu): D[M][N] = A[M][K] B[N][K]^T
+// in FP32, accumulated over all of K in tensor memory; M % 128 == 0,
+// N % 256 == 0, K % 128 == 0.
+cudaError_t launch_unpromoted_gemm(const uint8_t* a, const uint8_t* b, float* d, int64_t M, int64_t N, int64_t K,
+                                   uint64_t timeout_ns, cudaStream_t stream);
+
+// Reads and clears the diagnostic kernel's device status word.
+cudaError_t diag_take_status(int* status);
+
 }  // namespace fp8bs

@@ -228,6 +228,24 @@ int fp8bs_get_device_status(void* stream);
  * stays usable.  Returns FP8BS_OK once the kernel is launched. */
 int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream);
 
+/*
+ * Diagnostic, not part of the hot path: D = A B^T with the FP8 products of
+ * all of K accumulated by the tensor core alone (no promotion to FP32
+ * registers every 128 K, no scales), the configuration whose accumulation
+ * precision DeepSeek-V3 §3.3.2 "Increasing accumulation precision" measures
+ * (a maximum relative error near 2% for K = 4096 on H800).  Comparing its
+ * result with the exact sum gives the same measurement on this GPU.
+ *
+ *   a  [M][K] E4M3, K-major;  b  [N][K] E4M3, K-major;  d  [M][N] float32.
+ * Rules: M % 128 == 0, N % 256 == 0, K % 128 == 0, K > 0 (FP8BS_ERR_SHAPE);
+ * pointers 16-byte aligned (FP8BS_ERR_ALIGNMENT).  Asynchronous on
+ * `stream`; a bounded wait that expires records FP8BS_ERR_TIMEOUT for
+ * fp8bs_get_device_status() and leaves d unwritten.  Caller owns all
+ * buffers.
+ */
+int fp8bs_diag_gemm_unpromoted(const uint8_t* a, const uint8_t* b, float* d, int64_t M, int64_t N, int64_t K,
+                               void* stream);
+
 /* Sets the limit of every bounded device wait, in milliseconds (default
  * 2000; 0 restores the default).  Applies to launches made after the call. */
 int fp8bs_set_wait_timeout_ms(int64_t ms);

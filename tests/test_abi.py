@@ -117,6 +117,18 @@ def test_grouped_gemm_argument_errors(lib):
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
 
 
+def test_diag_unpromoted_argument_errors(lib):
+    g = lib.fp8bs_diag_gemm_unpromoted
+    assert g(FAKE, FAKE, FAKE, 128, 256, 100, None) == 2    # K % 128
+    assert g(FAKE, FAKE, FAKE, 128, 128, 128, None) == 2    # N % 256
+    assert g(FAKE, FAKE, FAKE, 100, 256, 128, None) == 2    # M % 128
+    assert g(FAKE, FAKE, FAKE, 128, 256, 0, None) == 2      # K == 0
+    assert g(FAKE, FAKE, FAKE, -128, 256, 128, None) == 1
+    assert g(None, FAKE, FAKE, 128, 256, 128, None) == 1
+    assert g(FAKE, FAKE, FAKE + 4, 128, 256, 128, None) == 3
+    assert g(None, None, None, 0, 256, 128, None) == 0     # empty: no-op
+
+
 def test_selftest_argument_errors(lib):
     assert lib.fp8bs_selftest_wait_timeout(0, None) == 1
     assert lib.fp8bs_selftest_wait_timeout(20000000, None) == 1
