@@ -7,26 +7,30 @@
 // multiplied by the two scales and accumulated; §3.5.2 names the cost of
 // that data movement), mapped onto Blackwell:
 //
-//   * a persistent, warp-specialised CTA per SM: warp 0 issues TMA loads of
-//     128x128 A and BNx128 B tiles into a shared-memory ring; warp 1 issues
-//     the MMAs (4 x tcgen05.mma K=32 per 128-K block) into one of two TMEM
-//     partial buffers, the first of the four overwriting the buffer; warp 2
-//     copies each k-block's scales (128 row scales of A, the B scales of
-//     the tile's columns) into a shared-memory scale ring with cp.async;
-//     warps 4-11 (two warpgroups) fold each finished partial into FP32
-//     registers with the block's scales (acc += P_kb * s_a * s_b) while the
-//     tensor core computes the next block into the other buffer;
+//   * a persistent, warp-specialised CTA per SM (or per SM of a CTA pair
+//     running the 2-SM MMA over 256-row tiles): warp 0 issues TMA loads of
+//     128x128 A and B tiles into a shared-memory ring; warps 1 and 3 issue
+//     the MMAs of alternate k-blocks (4 x tcgen05.mma K=32 per 128-K block)
+//     into one of two TMEM partial buffers, the first of the four
+//     overwriting the buffer; warp 2 copies each k-block's scales (128 row
+//     scales of A, the B scales of the tile's columns) into a shared-memory
+//     scale ring with cp.async; warps 4-11 (two warpgroups) fold each
+//     finished partial into FP32 registers with the block's scales
+//     (acc += P_kb * s_a * s_b) while the tensor core computes the next
+//     block into the other buffer;
 //   * the running FP32 accumulator never leaves the registers; each thread
 //     owns one output row (its TMEM lane) and BN/2 columns.  A TMEM buffer
 //     is released as soon as its last columns are in registers, before the
-//     last multiply-adds;
+//     last multiply-adds.  At the end of a tile each warp stages its rows in
+//     shared memory and TMA stores them, so the write drains while the warp
+//     folds the next tile;
 //   * mbarrier pipelines (operand ring, scale ring, TMEM buffers) with
 //     bounded waits; a timeout records a status and unwinds.
 //
 // The same kernel serves the dense GEMM (one group) and the grouped MoE
 // GEMM (per-expert row segments whose offsets are multiples of 128, read
-// from device memory; the expert index selects B's slice through a 3-D
-// tensor map).
+// from device memory; CTA pairs are formed inside each segment; the expert
+// index selects B's slice through a 3-D tensor map).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
