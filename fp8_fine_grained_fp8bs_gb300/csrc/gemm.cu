@@ -218,7 +218,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // Work unit t -> (first row, first column, group, end of the rows the
-// unit may write).  Units run m-tile-major with the BN-wide n-tiles of one
+// unit may write); g carries the group of the caller's previous unit in.  Units run m-tile-major with the BN-wide n-tiles of one
 // m-tile consecutive, so concurrently running CTAs share A rows.
 //
 // With CTA pairs (a cluster of two running one 2-SM MMA over a 256-row
@@ -246,12 +246,10 @@ __device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const 
     row_end = M;
     return;
   }
-  int lo = 0, hi = num_groups - 1;  // last g with cum[g] <= mu
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_cum[mid] <= mu) lo = mid; else hi = mid - 1;
-  }
-  g = lo;
+  // last g with cum[g] <= mu.  A CTA's units only move forward, so the
+  // search resumes from the group of its previous unit (g on entry, 0 for
+  // the first): usually no step, a few shared loads at most.
+  while (g + 1 < num_groups && s_cum[g + 1] <= mu) ++g;
   const int local = kPair ? 2 * (mu - s_cum[g]) + static_cast<int>(rank) : mu - s_cum[g];
   row0 = s_off[g] + local * kBlockM;
   row_end = s_off[g + 1];
@@ -362,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool live = true;
       int issued = 0;
+      int g = 0;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
-        int row0, n0, g;
+        int row0, n0;
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
@@ -473,8 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // final step).
       uint32_t step = 0;
       bool live = true;
+      int g = 0;
       for (int t = unit0; t < total_tiles && live; t += nunits) {
-        int row0, n0, g;
+        int row0, n0;
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         const bool last_tile = t + nunits >= total_tiles;
@@ -526,8 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t buf = 0, tphase = 0;
     uint32_t step = 0;
     bool live = true;
+    int g = 0;
     for (int t = unit0; t < total_tiles && live; t += nunits) {
-      int row0, n0, g;
+      int row0, n0;
       int64_t row_end;
       tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
       const int ncol0 = n0 + colhalf * C::kColsPerThread;
