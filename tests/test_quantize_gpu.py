@@ -140,3 +140,39 @@ def test_full_size_standalone_quantize_sampled():
     # every non-zero group's absmax element maps to +-448 (property at full size)
     q = to_host(xq).reshape(16384, 56, 128)
     assert np.all(np.any((q == 0x7E) | (q == 0xFE), axis=2))
+
+
+def test_full_size_dual_quantize_sampled():
+    """X[16384, 7168] in both layouts, as the benchmark's dual line quantises
+    it: 1x128 groups on sampled rows, 128x1 groups on sampled row blocks
+    (each 128-row block's column groups are independent of the others)."""
+    torch, fp8bs = require_gpu()
+    bits = synth.quantize_input(0)
+    xq, sx, xq_t, sx_t = fp8bs.quantize_act(to_dev_bf16(bits), transposed=True)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(0, 16384, 211), [16383]]))
+    q_ref, s_ref = oracle.quantize_act_1x128(bits[rows])
+    assert_bytes_equal(to_host(xq)[rows], q_ref, "1x128 codes")
+    assert_scales_equal(to_host(sx).T[rows], s_ref, "1x128 scales")
+    qt, st = to_host(xq_t), to_host(sx_t)
+    for rb in (0, 37, 127):
+        qt_ref, st_ref = oracle.quantize_act_128x1(bits[128 * rb:128 * (rb + 1)])
+        assert_bytes_equal(qt[:, 128 * rb:128 * (rb + 1)], qt_ref, f"128x1 codes, row block {rb}")
+        assert_scales_equal(st[rb][:, None], st_ref, f"128x1 scales, row block {rb}")
+
+
+def test_full_size_weight_with_transposed_copy_sampled():
+    """W[7168, 7168] with the transposed copy (the shape and launch of the
+    benchmark's weight line, seeded N(0, 0.02) weights); sampled 128-row
+    block rows checked in both layouts."""
+    torch, fp8bs = require_gpu()
+    w_bits = synth.normal_bf16((7168, 7168), 0.02, 0, 2)
+    wq, sw, wq_t, sw_t = fp8bs.quantize_weight(to_dev_bf16(w_bits), transposed=True)
+    torch.cuda.synchronize()
+    q, s, qt, st = to_host(wq), to_host(sw), to_host(wq_t), to_host(sw_t)
+    for nb in (0, 23, 55):
+        q_ref, s_ref = oracle.quantize_weight_128x128(w_bits[128 * nb:128 * (nb + 1)])
+        assert_bytes_equal(q[128 * nb:128 * (nb + 1)], q_ref, f"codes, block row {nb}")
+        assert_scales_equal(s[nb:nb + 1], s_ref, f"scales, block row {nb}")
+        assert_bytes_equal(qt[:, 128 * nb:128 * (nb + 1)], q_ref.T, f"transposed codes, block row {nb}")
+        assert_scales_equal(st[:, nb:nb + 1], s_ref.T, f"transposed scales, block row {nb}")
