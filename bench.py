@@ -221,7 +221,11 @@ def _time_ms(fn, stream, warmup: int, reps: int) -> float:
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm_peak: float, warmup: int):
+WORKLOAD_SECTIONS = ("dgrad", "wgrad", "context", "weight", "moe")
+
+
+def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm_peak: float, warmup: int,
+                      sections=WORKLOAD_SECTIONS):
     """The other configurations of the path, each kernel timed alone.
 
     * MoE grouped fprop: 8192 tokens, top-8 of 32 experts (Zipf s=1.1),
@@ -250,138 +254,146 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"gbs": gbs, "ms": ms, "frac_of_hbm": gbs / hbm_peak, "bytes": nbytes, **extra}
 
-    # ---- dgrad
-    dy_bits, w_bits = synth.dgrad(seed=rank)
-    dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    w = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    dyq, sdy = fp8bs.quantize_act(dy)
-    _, _, wq_t, sw_t = fp8bs.quantize_weight(w, transposed=True)
-    dx = torch.empty((4096, 2048), dtype=torch.float32, device=dev)
-    ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq, sdy, wq_t, sw_t, fp8bs.SCALE_BLOCK128x128, dx, fp8bs.OUT_F32,
-                                           4096, 2048, 7168, 0, stream), stream, warmup, reps)
-    out["dgrad"] = gemm_line(2.0 * 4096 * 2048 * 7168, ms, shape="M=4096 N=2048 K=7168, FP32 out")
-    del dy, w, dyq, sdy, wq_t, sw_t, dx
+    if "dgrad" in sections:
+        # ---- dgrad
+        dy_bits, w_bits = synth.dgrad(seed=rank)
+        dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        w = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        dyq, sdy = fp8bs.quantize_act(dy)
+        _, _, wq_t, sw_t = fp8bs.quantize_weight(w, transposed=True)
+        dx = torch.empty((4096, 2048), dtype=torch.float32, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq, sdy, wq_t, sw_t, fp8bs.SCALE_BLOCK128x128, dx, fp8bs.OUT_F32,
+                                               4096, 2048, 7168, 0, stream), stream, warmup, reps)
+        out["dgrad"] = gemm_line(2.0 * 4096 * 2048 * 7168, ms, shape="M=4096 N=2048 K=7168, FP32 out")
+        del dy, w, dyq, sdy, wq_t, sw_t, dx
 
-    # ---- wgrad (+ the dual-layout quantize of its operands)
-    dy_bits, x_bits = synth.wgrad(seed=rank)
-    dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    _, _, dyq_t, sdy_t = fp8bs.quantize_act(dy, transposed=True)
-    xq, sx, xq_t, sx_t = fp8bs.quantize_act(x, transposed=True)
-    dw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
-    ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq_t, sdy_t, xq_t, sx_t, fp8bs.SCALE_ROW1x128, dw, fp8bs.OUT_F32,
-                                           2048, 7168, 16384, 0, stream), stream, warmup, reps)
-    out["wgrad"] = gemm_line(2.0 * 2048 * 7168 * 16384, ms, shape="M=2048 N=7168 K=T=16384, row-scaled B, FP32 out")
-    T_, K_ = x.shape
-    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act(x, T_, K_, K_, xq, sx, xq_t, sx_t, stream), stream, warmup, reps)
-    out["quantize_dual"] = bw_line(T_ * K_ * (2 + 1 + 1) + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
-                                   shape="X[16384,7168] -> 1x128 and 128x1")
-    # power-of-two scales (§3.3.3 (1)) and the FP8 re-tiling 1x128 -> 128x1 (§3.5.2) of the same X
-    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act_ex(x, T_, K_, K_, xq, sx, None, None, fp8bs.SCALE_POW2, stream),
-                  stream, warmup, reps)
-    out["quantize_pow2"] = bw_line(T_ * K_ * (2 + 1) + T_ * (K_ // 128) * 4, ms,
-                                   shape="X[16384,7168] -> 1x128, power-of-two scales")
-    ms = _time_ms(lambda: fp8bs.fp8bs_requant_1x128_to_128x1(xq, sx, T_, K_, xq_t, sx_t, fp8bs.SCALE_POW2, stream),
-                  stream, warmup, reps)
-    out["requant_1x128_to_128x1"] = bw_line(T_ * K_ * 2 + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
-                                            shape="X[16384,7168] FP8 1x128 -> 128x1 (dequantise, transpose, "
-                                                  "requantise), power-of-two scales")
-    del dy, x, dyq_t, sdy_t, xq, sx, xq_t, sx_t, dw
+    if "wgrad" in sections:
+        # ---- wgrad (+ the dual-layout quantize of its operands)
+        dy_bits, x_bits = synth.wgrad(seed=rank)
+        dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        _, _, dyq_t, sdy_t = fp8bs.quantize_act(dy, transposed=True)
+        xq, sx, xq_t, sx_t = fp8bs.quantize_act(x, transposed=True)
+        dw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_gemm(dyq_t, sdy_t, xq_t, sx_t, fp8bs.SCALE_ROW1x128, dw, fp8bs.OUT_F32,
+                                               2048, 7168, 16384, 0, stream), stream, warmup, reps)
+        out["wgrad"] = gemm_line(2.0 * 2048 * 7168 * 16384, ms, shape="M=2048 N=7168 K=T=16384, row-scaled B, FP32 out")
+        T_, K_ = x.shape
+        ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act(x, T_, K_, K_, xq, sx, xq_t, sx_t, stream), stream, warmup, reps)
+        out["quantize_dual"] = bw_line(T_ * K_ * (2 + 1 + 1) + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
+                                       shape="X[16384,7168] -> 1x128 and 128x1")
+        # power-of-two scales (§3.3.3 (1)) and the FP8 re-tiling 1x128 -> 128x1 (§3.5.2) of the same X
+        ms = _time_ms(lambda: fp8bs.fp8bs_quantize_act_ex(x, T_, K_, K_, xq, sx, None, None, fp8bs.SCALE_POW2, stream),
+                      stream, warmup, reps)
+        out["quantize_pow2"] = bw_line(T_ * K_ * (2 + 1) + T_ * (K_ // 128) * 4, ms,
+                                       shape="X[16384,7168] -> 1x128, power-of-two scales")
+        ms = _time_ms(lambda: fp8bs.fp8bs_requant_1x128_to_128x1(xq, sx, T_, K_, xq_t, sx_t, fp8bs.SCALE_POW2, stream),
+                      stream, warmup, reps)
+        out["requant_1x128_to_128x1"] = bw_line(T_ * K_ * 2 + (T_ * (K_ // 128) + K_ * (T_ // 128)) * 4, ms,
+                                                shape="X[16384,7168] FP8 1x128 -> 128x1 (dequantise, transpose, "
+                                                      "requantise), power-of-two scales")
+        del dy, x, dyq_t, sdy_t, xq, sx, xq_t, sx_t, dw
 
-    # ---- context only (not part of the path): the library BF16 GEMM on the
-    # dense fprop shape, to set the "FP8 ~ 2x BF16" claim of the pages beside
-    # the block-scaled FP8 GEMM
-    g0 = torch.Generator(device=dev)
-    g0.manual_seed(2000 + rank)
-    xa = torch.randn((4096, 7168), generator=g0, device=dev).to(torch.bfloat16)
-    wa = (torch.randn((7168, 7168), generator=g0, device=dev) * 0.02).to(torch.bfloat16)
-    ya = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
-    ms = _time_ms(lambda: torch.matmul(xa, wa.t(), out=ya), stream, warmup, reps)
-    out["context_bf16_matmul"] = gemm_line(2.0 * 4096 * 7168 * 7168, ms,
-                                           shape="torch.matmul BF16 4096x7168x7168 (cuBLAS), context only")
-    out["context_bf16_matmul"]["frac_of_bf16_peak"] = out["context_bf16_matmul"]["tflops"] / (fp8_peak / 2.0)
-    del xa, wa, ya
+    if "context" in sections:
+        # ---- context only (not part of the path): the library BF16 GEMM on the
+        # dense fprop shape, to set the "FP8 ~ 2x BF16" claim of the pages beside
+        # the block-scaled FP8 GEMM
+        g0 = torch.Generator(device=dev)
+        g0.manual_seed(2000 + rank)
+        xa = torch.randn((4096, 7168), generator=g0, device=dev).to(torch.bfloat16)
+        wa = (torch.randn((7168, 7168), generator=g0, device=dev) * 0.02).to(torch.bfloat16)
+        ya = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: torch.matmul(xa, wa.t(), out=ya), stream, warmup, reps)
+        out["context_bf16_matmul"] = gemm_line(2.0 * 4096 * 7168 * 7168, ms,
+                                               shape="torch.matmul BF16 4096x7168x7168 (cuBLAS), context only")
+        out["context_bf16_matmul"]["frac_of_bf16_peak"] = out["context_bf16_matmul"]["tflops"] / (fp8_peak / 2.0)
+        del xa, wa, ya
 
-    # ---- context only: accumulation precision without promotion.  The pages
-    # (H800, all of K = 4096 accumulated in the tensor core) report a maximum
-    # relative error near 2%; the diagnostic GEMM accumulates all of K in
-    # tensor memory on this GPU, the production GEMM promotes every 128 K
-    # (block scales 1 here).  Reference: the float64 product of the decoded
-    # codes, exact for these sums (multiples of 2^-18 below 2^31).
-    Mc, Nc, Kc = 128, 256, 4096
-    ac = torch.randn((Mc, Kc), generator=g0, device=dev).to(torch.bfloat16)
-    bc = torch.randn((Nc, Kc), generator=g0, device=dev).to(torch.bfloat16)
-    acq, _ = fp8bs.quantize_act(ac, stream=stream)
-    bcq, _ = fp8bs.quantize_act(bc, stream=stream)
-    d_un = fp8bs.diag_gemm_unpromoted(acq, bcq, stream=stream)
-    d_pr = fp8bs.gemm(acq, torch.ones((Kc // 128, Mc), device=dev), bcq,
-                      torch.ones((Nc // 128, Kc // 128), device=dev), out_dtype=torch.float32, stream=stream)
-    torch.cuda.synchronize(dev)
-    yc = acq.view(torch.float8_e4m3fn).double() @ bcq.view(torch.float8_e4m3fn).double().t()
-    big = yc.abs() >= 0.1 * yc.pow(2).mean().sqrt()
+    if "context" in sections:
+        # ---- context only: accumulation precision without promotion.  The pages
+        # (H800, all of K = 4096 accumulated in the tensor core) report a maximum
+        # relative error near 2%; the diagnostic GEMM accumulates all of K in
+        # tensor memory on this GPU, the production GEMM promotes every 128 K
+        # (block scales 1 here).  Reference: the float64 product of the decoded
+        # codes, exact for these sums (multiples of 2^-18 below 2^31).
+        Mc, Nc, Kc = 128, 256, 4096
+        ac = torch.randn((Mc, Kc), generator=g0, device=dev).to(torch.bfloat16)
+        bc = torch.randn((Nc, Kc), generator=g0, device=dev).to(torch.bfloat16)
+        acq, _ = fp8bs.quantize_act(ac, stream=stream)
+        bcq, _ = fp8bs.quantize_act(bc, stream=stream)
+        d_un = fp8bs.diag_gemm_unpromoted(acq, bcq, stream=stream)
+        d_pr = fp8bs.gemm(acq, torch.ones((Kc // 128, Mc), device=dev), bcq,
+                          torch.ones((Nc // 128, Kc // 128), device=dev), out_dtype=torch.float32, stream=stream)
+        torch.cuda.synchronize(dev)
+        yc = acq.view(torch.float8_e4m3fn).double() @ bcq.view(torch.float8_e4m3fn).double().t()
+        big = yc.abs() >= 0.1 * yc.pow(2).mean().sqrt()
 
-    def acc_err(d):
-        e = (d.double() - yc).abs()
-        return {"max_err_over_max_abs": float(e.max() / yc.abs().max()),
-                "max_rel_err": float((e[big] / yc[big].abs()).max())}
+        def acc_err(d):
+            e = (d.double() - yc).abs()
+            return {"max_err_over_max_abs": float(e.max() / yc.abs().max()),
+                    "max_rel_err": float((e[big] / yc[big].abs()).max())}
 
-    out["context_unpromoted_accumulation"] = {
-        "shape": f"{Mc}x{Nc}x{Kc}, E4M3 codes of N(0,1) in 1x128 groups, scales left out",
-        "unpromoted_tensor_core": acc_err(d_un), "promoted_every_128": acc_err(d_pr),
-        "pages_h800_unpromoted_max_rel_err": 0.02}
-    del ac, bc, acq, bcq, d_un, d_pr, yc, big
+        out["context_unpromoted_accumulation"] = {
+            "shape": f"{Mc}x{Nc}x{Kc}, E4M3 codes of N(0,1) in 1x128 groups, scales left out",
+            "unpromoted_tensor_core": acc_err(d_un), "promoted_every_128": acc_err(d_pr),
+            "pages_h800_unpromoted_max_rel_err": 0.02}
+        del ac, bc, acq, bcq, d_un, d_pr, yc, big
 
-    # ---- weight quantize with the transposed copy
+    # one generator for the weight and MoE sections (the MoE weights follow W
+    # in its stream when both run)
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + rank)
-    wbig = (torch.randn((7168, 7168), generator=g, device=dev) * 0.02).to(torch.bfloat16)
-    wq, sw, wq_t2, sw_t2 = fp8bs.quantize_weight(wbig, transposed=True)
-    ms = _time_ms(lambda: fp8bs.fp8bs_quantize_weight(wbig, 7168, 7168, 7168, wq, sw, wq_t2, sw_t2, stream),
-                  stream, warmup, reps)
-    out["quantize_weight"] = bw_line(7168 * 7168 * (2 + 1 + 1) + 2 * 56 * 56 * 4, ms,
-                                     shape="W[7168,7168] -> 128x128 blocks + transposed copy")
-    del wbig, wq, sw, wq_t2, sw_t2
+    if "weight" in sections:
+        # ---- weight quantize with the transposed copy
+        wbig = (torch.randn((7168, 7168), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        wq, sw, wq_t2, sw_t2 = fp8bs.quantize_weight(wbig, transposed=True)
+        ms = _time_ms(lambda: fp8bs.fp8bs_quantize_weight(wbig, 7168, 7168, 7168, wq, sw, wq_t2, sw_t2, stream),
+                      stream, warmup, reps)
+        out["quantize_weight"] = bw_line(7168 * 7168 * (2 + 1 + 1) + 2 * 56 * 56 * 4, ms,
+                                         shape="W[7168,7168] -> 128x128 blocks + transposed copy")
+        del wbig, wq, sw, wq_t2, sw_t2
 
-    # ---- MoE grouped fprop
-    E, H, I = 32, 7168, 2048
-    choice = synth.moe_routing(seed=rank)
-    offsets_np, src_np = synth.moe_layout(choice, E)
-    rows = int(offsets_np[-1])
-    real_rows = int((src_np >= 0).sum())
-    x_tok = torch.from_numpy(synth.normal_bf16((8192, H), 1.0, rank, synth.TID_X, outliers=True).view(np.int16))
-    x_tok = x_tok.view(torch.bfloat16).to(dev)
-    src = torch.from_numpy(src_np).to(dev)
-    x_rows = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
-    ok = src >= 0
-    x_rows[ok] = x_tok[src[ok]]
-    offsets = torch.from_numpy(offsets_np).to(dev)
-    w_gu = (torch.randn((E * 2 * I, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
-    w_dn = (torch.randn((E * H, I), generator=g, device=dev) * 0.02).to(torch.bfloat16)
-    d_in = torch.randn((rows, I), generator=g, device=dev).to(torch.bfloat16)
-    d_in[~ok] = 0
-    aq, sa = fp8bs.quantize_act(x_rows)
-    bq, sb = fp8bs.quantize_weight(w_gu)
-    y1 = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
-    ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y1, fp8bs.OUT_BF16, 2 * I, H,
-                                                   stream), stream, warmup, reps)
-    out["moe_gate_up"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
-                                   shape=f"grouped 32 experts, [{rows} x {2 * I} x {H}], BF16 out")
-    # fused SwiGLU -> 1x128 quantise of the gate/up output (the down projection's input)
-    sq = torch.empty((rows, I), dtype=torch.uint8, device=dev)
-    ss = torch.empty((I // 128, rows), dtype=torch.float32, device=dev)
-    ms = _time_ms(lambda: fp8bs.fp8bs_swiglu_quantize(y1, rows, I, 2 * I, sq, ss, fp8bs.SCALE_ABSMAX, stream),
-                  stream, warmup, reps)
-    out["swiglu_quantize"] = bw_line(rows * (2 * I * 2 + I + (I // 128) * 4), ms,
-                                     shape=f"[{rows} x {2 * I}] BF16 gate|up -> SwiGLU -> 1x128 E4M3 [{rows} x {I}]")
-    del aq, sa, bq, sb, y1, x_rows, w_gu, sq, ss
-    aq, sa = fp8bs.quantize_act(d_in)
-    bq, sb = fp8bs.quantize_weight(w_dn)
-    y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
-    ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y2, fp8bs.OUT_BF16, H, I,
-                                                   stream), stream, warmup, reps)
-    out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
-                                shape=f"grouped 32 experts, [{rows} x {H} x {I}], BF16 out")
-    del aq, sa, bq, sb, y2, d_in, w_dn
+    if "moe" in sections:
+        # ---- MoE grouped fprop
+        E, H, I = 32, 7168, 2048
+        choice = synth.moe_routing(seed=rank)
+        offsets_np, src_np = synth.moe_layout(choice, E)
+        rows = int(offsets_np[-1])
+        real_rows = int((src_np >= 0).sum())
+        x_tok = torch.from_numpy(synth.normal_bf16((8192, H), 1.0, rank, synth.TID_X, outliers=True).view(np.int16))
+        x_tok = x_tok.view(torch.bfloat16).to(dev)
+        src = torch.from_numpy(src_np).to(dev)
+        x_rows = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
+        ok = src >= 0
+        x_rows[ok] = x_tok[src[ok]]
+        offsets = torch.from_numpy(offsets_np).to(dev)
+        w_gu = (torch.randn((E * 2 * I, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        w_dn = (torch.randn((E * H, I), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        d_in = torch.randn((rows, I), generator=g, device=dev).to(torch.bfloat16)
+        d_in[~ok] = 0
+        aq, sa = fp8bs.quantize_act(x_rows)
+        bq, sb = fp8bs.quantize_weight(w_gu)
+        y1 = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y1, fp8bs.OUT_BF16, 2 * I, H,
+                                                       stream), stream, warmup, reps)
+        out["moe_gate_up"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
+                                       shape=f"grouped 32 experts, [{rows} x {2 * I} x {H}], BF16 out")
+        # fused SwiGLU -> 1x128 quantise of the gate/up output (the down projection's input)
+        sq = torch.empty((rows, I), dtype=torch.uint8, device=dev)
+        ss = torch.empty((I // 128, rows), dtype=torch.float32, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_swiglu_quantize(y1, rows, I, 2 * I, sq, ss, fp8bs.SCALE_ABSMAX, stream),
+                      stream, warmup, reps)
+        out["swiglu_quantize"] = bw_line(rows * (2 * I * 2 + I + (I // 128) * 4), ms,
+                                         shape=f"[{rows} x {2 * I}] BF16 gate|up -> SwiGLU -> 1x128 E4M3 [{rows} x {I}]")
+        del aq, sa, bq, sb, y1, x_rows, w_gu, sq, ss
+        aq, sa = fp8bs.quantize_act(d_in)
+        bq, sb = fp8bs.quantize_weight(w_dn)
+        y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y2, fp8bs.OUT_BF16, H, I,
+                                                       stream), stream, warmup, reps)
+        out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
+                                    shape=f"grouped 32 experts, [{rows} x {H} x {I}], BF16 out")
+        del aq, sa, bq, sb, y2, d_in, w_dn
     if fp8bs.fp8bs_get_device_status(stream) != 0:
         raise RuntimeError("device status after the workload measurements")
     torch.cuda.empty_cache()
@@ -397,6 +409,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-kernel lines of the MoE, dgrad, wgrad and quantize variants")
+    ap.add_argument("--workloads", default=",".join(WORKLOAD_SECTIONS),
+                    help="comma-separated sections of the per-kernel lines to run: " + ", ".join(WORKLOAD_SECTIONS)
+                         + " (wgrad also times the dual, power-of-two and re-tiling quantisations of its X; "
+                           "moe the grouped GEMMs and the fused SwiGLU quantisation)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -563,7 +579,12 @@ def main():
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     workloads = None
     if not args.no_workloads:
-        workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup)
+        sections = tuple(w for w in args.workloads.split(",") if w)
+        unknown = set(sections) - set(WORKLOAD_SECTIONS)
+        if unknown:
+            raise SystemExit(f"unknown workload sections: {sorted(unknown)}")
+        workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup,
+                                      sections)
     gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
     value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
