@@ -1,9 +1,9 @@
 """Benchmark of the fine-grained FP8 hot path on GB300.
 
 One step = the FP8 Linear forward of the dense workload with online
-quantisation (DeepSeek-V3 §3.3): quantise X[4096,7168] (BF16, 1x128 tiles),
-quantise W[7168,7168] (BF16, 128x128 blocks), block-scaled FP8 GEMM
-Y = X W^T with BF16 output.  ``value`` is the step's GEMM FLOPs
+quantisation (DeepSeek-V3 §3.3): quantise X[4096,7168] (BF16, 1x128 tiles)
+and W[7168,7168] (BF16, 128x128 blocks) in one launch, block-scaled FP8
+GEMM Y = X W^T with BF16 output.  ``value`` is the step's GEMM FLOPs
 (2*M*N*K) per second over the whole step, in TFLOP/s.  Measured in the same
 run and reported beside it:
   * ``gemm``:     the GEMM kernel alone (CUDA events around each launch);
@@ -457,16 +457,10 @@ def main():
     sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
-    # The two quantisations are independent: W's runs on a second stream
-    # beside X's (both stream HBM; together they leave no half-empty last
-    # wave), and the GEMM waits for both.
-    s_w = torch.cuda.Stream(dev)
-
+    # X (1x128) and W (128x128) are quantised by one launch whose persistent
+    # grid walks X's tiles, then W's; then the GEMM.
     def step(gemm_events=None):
-        s_w.wait_stream(stream)                     # the previous GEMM is done with wq
-        fp8bs.fp8bs_quantize_weight(win, N, K, K, wq, sw, None, None, s_w)
-        fp8bs.fp8bs_quantize_act(xin, M, K, K, xq, sx, None, None, stream)
-        stream.wait_stream(s_w)
+        fp8bs.fp8bs_quantize_act_weight(xin, M, K, K, xq, sx, win, N, K, K, wq, sw, fp8bs.SCALE_ABSMAX, stream)
         if gemm_events is not None:
             gemm_events[0].record(stream)
         fp8bs.fp8bs_gemm(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, y, fp8bs.OUT_BF16, M, N, K, 0, stream)
@@ -549,8 +543,8 @@ def main():
             stream.wait_event(ev_in[i])
             if i >= 2:
                 stream.wait_event(ev_out[i - 2])             # yb[j] read out
-            fp8bs.fp8bs_quantize_act(xb[j], M, K, K, xqb[j], sxb[j], None, None, stream)
-            fp8bs.fp8bs_quantize_weight(wb[j], N, K, K, wqb[j], swb[j], None, None, stream)
+            fp8bs.fp8bs_quantize_act_weight(xb[j], M, K, K, xqb[j], sxb[j], wb[j], N, K, K, wqb[j], swb[j],
+                                            fp8bs.SCALE_ABSMAX, stream)
             fp8bs.fp8bs_gemm(xqb[j], sxb[j], wqb[j], swb[j], fp8bs.SCALE_BLOCK128x128, yb[j], fp8bs.OUT_BF16,
                              M, N, K, 0, stream)
             ev_comp[i].record(stream)
@@ -620,7 +614,7 @@ def main():
         "e2e": {"value": world * GEMM_FLOP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(xin.numel() * 2 + win.numel() * 2),
                 "d2h_bytes_per_step": int(y.numel() * 2), "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
     if workloads is not None:

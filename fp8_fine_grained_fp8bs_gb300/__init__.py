@@ -22,7 +22,7 @@ from .build import LIB_PATH, build as _build
 __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
-    "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
+    "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_quantize_act_weight", "quantize_act_weight", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string", "fp8bs_selftest_wait_timeout",
     "fp8bs_diag_gemm_unpromoted", "diag_gemm_unpromoted",
     "quantize_act", "quantize_weight", "gemm", "grouped_gemm", "requant_1x128_to_128x1", "swiglu_quantize",
@@ -53,6 +53,8 @@ _SIGNATURES = {
     "fp8bs_quantize_weight": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp],
     "fp8bs_quantize_act_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_quantize_weight_ex": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp],
+    "fp8bs_quantize_act_weight": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+                                  _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_requant_1x128_to_128x1": [_c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_swiglu_quantize": [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
     "fp8bs_gemm": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
@@ -168,6 +170,12 @@ def fp8bs_selftest_wait_timeout(timeout_us: int, stream=None):
     _check(load_library().fp8bs_selftest_wait_timeout(int(timeout_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
 
 
+def fp8bs_quantize_act_weight(x, M, K, ldx, xq, sx, w, N, Kw, ldw, wq, sw, scale_mode=0, stream=None):
+    _check(load_library().fp8bs_quantize_act_weight(_ptr(x), M, K, ldx, _ptr(xq), _ptr(sx), _ptr(w), N, Kw, ldw,
+                                                    _ptr(wq), _ptr(sw), int(scale_mode), _stream(stream)),
+           "fp8bs_quantize_act_weight")
+
+
 def fp8bs_diag_gemm_unpromoted(a, b, d, M, N, K, stream=None):
     _check(load_library().fp8bs_diag_gemm_unpromoted(_ptr(a), _ptr(b), _ptr(d), M, N, K, _stream(stream)),
            "fp8bs_diag_gemm_unpromoted")
@@ -273,3 +281,18 @@ def diag_gemm_unpromoted(a, b, stream=None):
     out = torch.empty((M, N), dtype=torch.float32, device=a.device)
     fp8bs_diag_gemm_unpromoted(a, b, out, M, N, K, stream)
     return out
+
+
+def quantize_act_weight(x, w, pow2: bool = False, stream=None):
+    """X [M,K] and W [N,Kw] bfloat16 CUDA tensors quantised in one launch:
+    returns (xq, sx [K/128, M], wq, sw [N/128, Kw/128])."""
+    import torch
+    M, K = x.shape
+    N, Kw = w.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    wq = torch.empty((N, Kw), dtype=torch.uint8, device=w.device)
+    sw = torch.empty((N // 128, Kw // 128), dtype=torch.float32, device=w.device)
+    fp8bs_quantize_act_weight(x, M, K, x.stride(0), xq, sx, w, N, Kw, w.stride(0), wq, sw,
+                              SCALE_POW2 if pow2 else SCALE_ABSMAX, stream)
+    return xq, sx, wq, sw

@@ -96,6 +96,29 @@ int fp8bs_quantize_weight_ex(const void* w, int64_t N, int64_t K, int64_t ldw, u
                                                  static_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_quantize_act_weight(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx,
+                              const void* w, int64_t N, int64_t Kw, int64_t ldw, uint8_t* wq, float* sw,
+                              int scale_mode, void* stream) {
+  if (M < 0 || K < 0 || ldx < K || N < 0 || Kw < 0 || ldw < Kw) return FP8BS_ERR_INVALID_ARG;
+  if (scale_mode != FP8BS_SCALE_ABSMAX && scale_mode != FP8BS_SCALE_POW2) return FP8BS_ERR_INVALID_ARG;
+  const bool x_empty = M == 0 || K == 0, w_empty = N == 0 || Kw == 0;
+  if (!x_empty && (x == nullptr || xq == nullptr || sx == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (!w_empty && (w == nullptr || wq == nullptr || sw == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0 || Kw % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 24) || N > (int64_t(1) << 24) || Kw > (int64_t(1) << 24))
+    return FP8BS_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(sx) || (ldx * 2) % 16 != 0) return FP8BS_ERR_ALIGNMENT;
+  if (!aligned16(w) || !aligned16(wq) || (ldw * 2) % 16 != 0) return FP8BS_ERR_ALIGNMENT;
+  if (x_empty && w_empty) return FP8BS_OK;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_quantize_act_weight(
+      static_cast<const uint16_t*>(x), x_empty ? 0 : M, K, ldx, xq, sx, static_cast<const uint16_t*>(w),
+      w_empty ? 0 : N, Kw, ldw, wq, sw, scale_mode == FP8BS_SCALE_POW2, sms, g_timeout_ns.load(),
+      static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq, float* sw, uint8_t* wq_t,
                           float* sw_t, void* stream) {
   return fp8bs_quantize_weight_ex(w, N, K, ldw, wq, sw, wq_t, sw_t, FP8BS_SCALE_ABSMAX, stream);

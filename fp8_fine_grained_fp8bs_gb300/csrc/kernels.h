@@ -20,6 +20,11 @@ cudaError_t launch_quantize_act_dual(const uint16_t* x, int64_t M, int64_t K, in
 cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* wq,
                                    float* sw, uint8_t* wq_t, float* sw_t, bool pow2, int sm_count,
                                    uint64_t timeout_ns, cudaStream_t stream);
+// One launch quantising X [M][K] in 1x128 groups and W [N][Kw] in 128x128
+// blocks (the two operands of an FP8 Linear); either may be empty (M or N 0).
+cudaError_t launch_quantize_act_weight(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx,
+                                       const uint16_t* w, int64_t N, int64_t Kw, int64_t ldw, uint8_t* wq, float* sw,
+                                       bool pow2, int sm_count, uint64_t timeout_ns, cudaStream_t stream);
 // FP8 -> FP8 re-tiling 1x128 -> 128x1 (dequantise, transpose, requantise);
 // plain loads, no waits.
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,

@@ -238,12 +238,13 @@ enum TileMode : int {
   kModeAct = 0,      // 1x128 groups, row layout
   kModeWeight = 1,   // one 128x128 group per tile, row layout
   kModeWeightT = 2,  // one 128x128 group per tile plus the transposed codes, block layout
-  kModeDual = 3      // 1x128 and 128x1 groups, block layout
+  kModeDual = 3,     // 1x128 and 128x1 groups, block layout
+  kModeActWeight = 4 // one launch over the tiles of X (1x128 groups) then of W (128x128), row layout
 };
 
 template <int kMode>
 struct QCfg {
-  static constexpr bool kRowLayout = kMode == kModeAct || kMode == kModeWeight;
+  static constexpr bool kRowLayout = kMode == kModeAct || kMode == kModeWeight || kMode == kModeActWeight;
   // block layouts also stage the transposed codes of a tile (16 KB) in
   // shared memory; two input stages keep two CTAs per SM
   static constexpr int kStages = kRowLayout ? 3 : 2;
@@ -324,9 +325,13 @@ __device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divis
     *reinterpret_cast<uint4*>(out + 16 * p) = make_uint4(cc[2 * p].x, cc[2 * p].y, cc[2 * p + 1].x, cc[2 * p + 1].y);
 }
 
+// Tiles [0, p.nrb * p.nkb) are p's tensor (read through tmx); with
+// kModeActWeight they are followed by pw's tensor (through tmw), quantised
+// in 128x128 groups.  Other modes ignore tmw and pw.
 template <int kMode>
 __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileParams p) {
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                      const TileParams p, const TileParams pw) {
   using Q = QCfg<kMode>;
   extern __shared__ uint8_t qsmem_raw[];
   // 1024-byte aligned base, offset from the shared array itself so that the
@@ -339,7 +344,8 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
   QShared& S = *reinterpret_cast<QShared*>(tiles + Q::kStages * kTileBytes + Q::kStageOutBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t ntiles = p.nrb * p.nkb;
+  const int64_t ntiles_x = p.nrb * p.nkb;
+  const int64_t ntiles = ntiles_x + (kMode == kModeActWeight ? pw.nrb * pw.nkb : 0);
   const int64_t K = static_cast<int64_t>(p.nkb) * kGroup;
 
   if (threadIdx.x == 0) {
@@ -354,7 +360,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 
   if (warp == kQComputeThreads / 32) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) prefetch_tmap(&tmx);
+    if (lane == 0) {
+      prefetch_tmap(&tmx);
+      if (kMode == kModeActWeight) prefetch_tmap(&tmw);
+    }
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -365,13 +374,17 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         break;
       }
       if (lane == 0) {
-        const int64_t rb = tile / p.nkb;
-        const int kb = static_cast<int>(tile - rb * p.nkb);
+        const bool second = kMode == kModeActWeight && tile >= ntiles_x;
+        const int64_t lt = second ? tile - ntiles_x : tile;
+        const int nkb = second ? pw.nkb : p.nkb;
+        const CUtensorMap* map = second ? &tmw : &tmx;
+        const int64_t rb = lt / nkb;
+        const int kb = static_cast<int>(lt - rb * nkb);
         uint8_t* dst = tiles + s * kTileBytes;
         mbar_arrive_expect_tx(&S.full[s], kTileBytes);
         if (Q::kRowLayout) {
-          tma_load_2d(dst, &tmx, &S.full[s], kb * kGroup, static_cast<int>(rb * kGroup));
-          tma_load_2d(dst + kTileBytes / 2, &tmx, &S.full[s], kb * kGroup + kGroup / 2, static_cast<int>(rb * kGroup));
+          tma_load_2d(dst, map, &S.full[s], kb * kGroup, static_cast<int>(rb * kGroup));
+          tma_load_2d(dst + kTileBytes / 2, map, &S.full[s], kb * kGroup + kGroup / 2, static_cast<int>(rb * kGroup));
         } else {
           tma_load_2d(dst, &tmx, &S.full[s], kb * kGroup, static_cast<int>(rb * kGroup));
         }
@@ -404,7 +417,14 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
   int64_t rb = static_cast<int64_t>(blockIdx.x) / p.nkb;
   int kb = static_cast<int>(blockIdx.x - rb * p.nkb);
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, par ^= 1u) {
-    if (tile != blockIdx.x) {
+    bool second = false;  // kModeActWeight: a tile of W
+    if (kMode == kModeActWeight) {
+      second = tile >= ntiles_x;
+      const int64_t lt = second ? tile - ntiles_x : tile;
+      const int nkb = second ? pw.nkb : p.nkb;
+      rb = lt / nkb;
+      kb = static_cast<int>(lt - rb * nkb);
+    } else if (tile != blockIdx.x) {
       rb += step_rb;
       kb += step_kb;
       if (kb >= p.nkb) { kb -= p.nkb; ++rb; }
@@ -435,8 +455,13 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       m = umax_halves(abs_bits(m));
       m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the other half of the row
       const int64_t row = rb * kGroup + r;
+      // the tensor this tile belongs to
+      const int64_t rows = second ? pw.rows : p.rows;
+      uint8_t* const q = second ? pw.q : p.q;
+      float* const sc = second ? pw.s : p.s;
+      const int64_t ld = second ? static_cast<int64_t>(pw.nkb) * kGroup : K;
       Divisor d;
-      if (kMode == kModeWeight) {
+      if (kMode == kModeWeight || second) {
 #pragma unroll
         for (int o = 2; o <= 16; o <<= 1) m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) S.red[par][warp] = m & 0xFFFFu;
@@ -448,16 +473,16 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 #pragma unroll
         for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
         d = group_divisor(S.tab, a, p.pow2 != 0);
-        if (t == 0) p.s[rb * p.nkb + kb] = d.s;
+        if (t == 0) sc[rb * (ld / kGroup) + kb] = d.s;
       } else {
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
           break;
         }
         d = group_divisor(S.tab, m & 0xFFFFu, p.pow2 != 0);
-        if (h == 0 && row < p.rows) p.s[static_cast<int64_t>(kb) * p.rows + row] = d.s;
+        if (h == 0 && row < rows) sc[static_cast<int64_t>(kb) * rows + row] = d.s;
       }
-      if (row < p.rows) quant_row64(w, d, h, p.q + row * K + static_cast<int64_t>(kb) * kGroup + 64 * h);
+      if (row < rows) quant_row64(w, d, h, q + row * ld + static_cast<int64_t>(kb) * kGroup + 64 * h);
       continue;
     }
 
@@ -607,13 +632,22 @@ bool encode_bf16_tiles(CUtensorMap* map, const uint16_t* base, int64_t rows, int
   return r == CUDA_SUCCESS;
 }
 
+// One persistent launch over p's tiles (and, for kModeActWeight, then over
+// pw's tiles of the BF16 matrix w with leading dimension ldw).
 template <int kMode>
-cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int sm_count, cudaStream_t stream) {
-  const int64_t ntiles = p.nrb * p.nkb;
+cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int sm_count, cudaStream_t stream,
+                         const uint16_t* w = nullptr, int64_t ldw = 0, const TileParams* pw = nullptr) {
+  const int64_t ntiles = p.nrb * p.nkb + (pw != nullptr ? pw->nrb * pw->nkb : 0);
   if (ntiles <= 0) return cudaSuccess;
-  CUtensorMap map;
-  if (!encode_bf16_tiles(&map, x, p.rows, static_cast<int64_t>(p.nkb) * kGroup, ld, QCfg<kMode>::kRowLayout))
+  CUtensorMap map, map_w;
+  if (p.nrb > 0 &&
+      !encode_bf16_tiles(&map, x, p.rows, static_cast<int64_t>(p.nkb) * kGroup, ld, QCfg<kMode>::kRowLayout))
     return cudaErrorInvalidValue;
+  if (pw != nullptr && pw->nrb > 0 &&
+      !encode_bf16_tiles(&map_w, w, pw->rows, static_cast<int64_t>(pw->nkb) * kGroup, ldw, QCfg<kMode>::kRowLayout))
+    return cudaErrorInvalidValue;
+  if (p.nrb <= 0) map = map_w;  // never read: p has no tiles
+  if (pw == nullptr || pw->nrb <= 0) map_w = map;
   auto kern = quant_tile_kernel<kMode>;
   constexpr int smem = q_smem_bytes<kMode>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -626,7 +660,9 @@ cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int
   if (e != cudaSuccess) return e;
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   const int grid = static_cast<int>(ntiles < slots ? ntiles : slots);
-  kern<<<grid, kQThreads, smem, stream>>>(map, p);
+  TileParams none = p;
+  none.nrb = 0;
+  kern<<<grid, kQThreads, smem, stream>>>(map, map_w, p, pw != nullptr ? *pw : none);
   return cudaGetLastError();
 }
 
@@ -893,6 +929,16 @@ cudaError_t launch_quantize_weight(const uint16_t* w, int64_t N, int64_t K, int6
   const TileParams p{N, N / kGroup, static_cast<int>(K / kGroup), wq, sw, wq_t, sw_t, timeout_ns, pow2 ? 1 : 0};
   if (wq_t != nullptr) return launch_tiles<kModeWeightT>(w, ldw, p, sm_count, stream);
   return launch_tiles<kModeWeight>(w, ldw, p, sm_count, stream);
+}
+
+cudaError_t launch_quantize_act_weight(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, float* sx,
+                                       const uint16_t* w, int64_t N, int64_t Kw, int64_t ldw, uint8_t* wq, float* sw,
+                                       bool pow2, int sm_count, uint64_t timeout_ns, cudaStream_t stream) {
+  const TileParams p{M,       (M + kGroup - 1) / kGroup, static_cast<int>(K / kGroup), xq, sx, nullptr, nullptr,
+                     timeout_ns, pow2 ? 1 : 0};
+  const TileParams pw{N, N / kGroup, static_cast<int>(Kw / kGroup), wq, sw, nullptr, nullptr, timeout_ns,
+                      pow2 ? 1 : 0};
+  return launch_tiles<kModeActWeight>(x, ldx, p, sm_count, stream, w, ldw, &pw);
 }
 
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, int64_t K, uint8_t* xq_t,

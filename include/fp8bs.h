@@ -132,6 +132,25 @@ int fp8bs_quantize_weight_ex(const void* w, int64_t N, int64_t K, int64_t ldw,
                              int scale_mode, void* stream);
 
 /*
+ * Both operands of an FP8 Linear (Figure 6, the online quantisation of
+ * §3.3.2) in one launch: X in 1x128 groups exactly as fp8bs_quantize_act_ex
+ * without the transposed output, and W in 128x128 blocks exactly as
+ * fp8bs_quantize_weight_ex without the transposed copy, with one
+ * scale_mode for both.  Codes and scales are bit-identical to the two
+ * separate calls; one persistent grid walks X's tiles, then W's.
+ *
+ *   x  [M][ldx] BF16, K columns;  xq [M][K];  sx [K/128][M] (kb-major).
+ *   w  [N][ldw] BF16, Kw columns; wq [N][Kw]; sw [N/128][Kw/128].
+ * Rules: the union of the two calls' rules (K, N, Kw multiples of 128,
+ * 16-byte aligned pointers and leading dimensions); M == 0 or N == 0 leaves
+ * that operand out; errors as those calls.
+ */
+int fp8bs_quantize_act_weight(const void* x, int64_t M, int64_t K, int64_t ldx,
+                              uint8_t* xq, float* sx,
+                              const void* w, int64_t N, int64_t Kw, int64_t ldw,
+                              uint8_t* wq, float* sw, int scale_mode, void* stream);
+
+/*
  * Backward re-tiling from FP8 (§3.5.2 "support for transposed GEMM
  * operations": read the 1x128-quantised activations, dequantise, transpose,
  * requantise in 128x1 tiles; §3.3.3 "low-precision activations" (1): with

@@ -117,6 +117,29 @@ def test_grouped_gemm_argument_errors(lib):
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
 
 
+def test_quantize_act_weight_argument_errors(lib):
+    q = lib.fp8bs_quantize_act_weight
+    ok = (FAKE, 128, 256, 256, FAKE, FAKE, FAKE, 128, 256, 256, FAKE, FAKE, 0, None)
+
+    def call(**kw):
+        names = ["x", "M", "K", "ldx", "xq", "sx", "w", "N", "Kw", "ldw", "wq", "sw", "mode", "stream"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return q(*[args[n] for n in names])
+    assert call(K=100, ldx=100) == 2                 # K % 128
+    assert call(N=100) == 2                          # N % 128
+    assert call(Kw=100, ldw=100) == 2                # Kw % 128
+    assert call(ldx=128) == 1                        # ldx < K
+    assert call(ldw=128) == 1                        # ldw < Kw
+    assert call(mode=7) == 1                         # scale mode
+    assert call(x=None) == 1
+    assert call(sw=None) == 1
+    assert call(wq=FAKE + 8) == 3
+    assert call(ldx=260) == 3                        # ldx * 2 not a multiple of 16
+    assert call(M=-1) == 1
+    assert call(x=None, xq=None, sx=None, M=0, w=None, wq=None, sw=None, N=0) == 0   # both empty: no-op
+
+
 def test_diag_unpromoted_argument_errors(lib):
     g = lib.fp8bs_diag_gemm_unpromoted
     assert g(FAKE, FAKE, FAKE, 128, 256, 100, None) == 2    # K % 128

@@ -176,3 +176,58 @@ def test_full_size_weight_with_transposed_copy_sampled():
         assert_scales_equal(s[nb:nb + 1], s_ref, f"scales, block row {nb}")
         assert_bytes_equal(qt[:, 128 * nb:128 * (nb + 1)], q_ref.T, f"transposed codes, block row {nb}")
         assert_scales_equal(st[:, nb:nb + 1], s_ref.T, f"transposed scales, block row {nb}")
+
+
+def _check_act_weight(x_bits, w_bits, pow2=False, rows=None, nblocks=None):
+    """The one-launch quantisation of X (1x128) and W (128x128) against the
+    oracle (sampled X rows and W block rows at large sizes)."""
+    torch, fp8bs = require_gpu()
+    x = to_dev_bf16(x_bits) if x_bits.shape[0] else torch.empty(x_bits.shape, dtype=torch.bfloat16, device="cuda:0")
+    w = to_dev_bf16(w_bits) if w_bits.shape[0] else torch.empty(w_bits.shape, dtype=torch.bfloat16, device="cuda:0")
+    xq, sx, wq, sw = fp8bs.quantize_act_weight(x, w, pow2=pow2)
+    assert fp8bs.fp8bs_get_device_status() == 0
+    if x_bits.shape[0]:
+        r = np.arange(x_bits.shape[0]) if rows is None else rows
+        q_ref, s_ref = oracle.quantize_act_1x128(x_bits[r], pow2=pow2)
+        assert_bytes_equal(to_host(xq)[r], q_ref, "X codes")
+        assert_scales_equal(to_host(sx).T[r], s_ref, "X scales")
+    if w_bits.shape[0]:
+        nbs = np.arange(w_bits.shape[0] // 128) if nblocks is None else nblocks
+        q, s = to_host(wq), to_host(sw)
+        for nb in nbs:
+            q_ref, s_ref = oracle.quantize_weight_128x128(w_bits[128 * nb:128 * (nb + 1)], pow2=pow2)
+            assert_bytes_equal(q[128 * nb:128 * (nb + 1)], q_ref, f"W codes, block row {nb}")
+            assert_scales_equal(s[nb:nb + 1], s_ref, f"W scales, block row {nb}")
+    return xq, sx, wq, sw
+
+
+@pytest.mark.parametrize("M,K,N,Kw", [(128, 512, 256, 512), (3, 384, 128, 256), (257, 256, 384, 1024),
+                                      (0, 256, 256, 512), (130, 512, 0, 256)])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_act_weight_one_launch(M, K, N, Kw, pow2):
+    x = synth.normal_bf16((M, K), 1.0, 40 + M, 1, outliers=True)
+    w = synth.normal_bf16((N, Kw), 0.02, 40 + N, 2)
+    _check_act_weight(x, w, pow2)
+
+
+def test_act_weight_one_launch_edge_values():
+    x = np.concatenate([_edge_rows(384), synth.normal_bf16((121, 384), 1.0, 5, 1, outliers=True)])
+    wf = np.zeros((256, 256), np.float32)
+    wf[128:, :128] = -0.0
+    wf[:128, 128:] = np.arange(128 * 128, dtype=np.float32).reshape(128, 128) % 97 - 48
+    wf[128:, 128:] = 1e-37
+    _check_act_weight(x, synth.f32_to_bf16_bits(wf))
+
+
+def test_act_weight_one_launch_step_shape():
+    """The benchmark step's operands, X[4096,7168] and W[7168,7168]: sampled
+    rows and block rows against the oracle, and every byte identical to the
+    two separate quantisations."""
+    torch, fp8bs = require_gpu()
+    x_bits, w_bits = synth.dense_fprop(0)
+    xq, sx, wq, sw = _check_act_weight(x_bits, w_bits, rows=np.arange(0, 4096, 331),
+                                       nblocks=np.array([0, 29, 55]))
+    xq2, sx2 = fp8bs.quantize_act(to_dev_bf16(x_bits))
+    wq2, sw2 = fp8bs.quantize_weight(to_dev_bf16(w_bits))
+    assert torch.equal(xq, xq2) and torch.equal(sx, sx2)
+    assert torch.equal(wq, wq2) and torch.equal(sw, sw2)
