@@ -11,7 +11,9 @@
 // a division.
 //
 // Also here: the power-of-two scale mode (§3.3.3 "low-precision
-// activations" (1)), the FP8 re-tiling 1x128 -> 128x1 of the backward pass
+// activations" (1)), the one-launch quantisation of both operands of an FP8
+// Linear (X in 1x128 groups, then W in 128x128 blocks, by one persistent
+// tile grid), the FP8 re-tiling 1x128 -> 128x1 of the backward pass
 // (§3.5.2 "support for transposed GEMM operations"), and the fused SwiGLU ->
 // 1x128 quantisation of the MoE down projection's input (§3.3.3 (2)).
 #include <cuda_fp16.h>
