@@ -225,7 +225,7 @@ WORKLOAD_SECTIONS = ("dgrad", "wgrad", "context", "weight", "moe")
 
 
 def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm_peak: float, warmup: int,
-                      sections=WORKLOAD_SECTIONS):
+                      sections=WORKLOAD_SECTIONS, moe_tokens: int = 8192, moe_experts: int = 32):
     """The other configurations of the path, each kernel timed alone.
 
     * MoE grouped fprop: 8192 tokens, top-8 of 32 experts (Zipf s=1.1),
@@ -355,12 +355,13 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
 
     if "moe" in sections:
         # ---- MoE grouped fprop
-        E, H, I = 32, 7168, 2048
-        choice = synth.moe_routing(seed=rank)
+        E, H, I = moe_experts, 7168, 2048
+        choice = synth.moe_routing(seed=rank, tokens=moe_tokens, experts=E)
         offsets_np, src_np = synth.moe_layout(choice, E)
         rows = int(offsets_np[-1])
         real_rows = int((src_np >= 0).sum())
-        x_tok = torch.from_numpy(synth.normal_bf16((8192, H), 1.0, rank, synth.TID_X, outliers=True).view(np.int16))
+        x_tok = torch.from_numpy(synth.normal_bf16((moe_tokens, H), 1.0, rank, synth.TID_X,
+                                                   outliers=True).view(np.int16))
         x_tok = x_tok.view(torch.bfloat16).to(dev)
         src = torch.from_numpy(src_np).to(dev)
         x_rows = torch.zeros((rows, H), dtype=torch.bfloat16, device=dev)
@@ -377,7 +378,7 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
         ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y1, fp8bs.OUT_BF16, 2 * I, H,
                                                        stream), stream, warmup, reps)
         out["moe_gate_up"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
-                                       shape=f"grouped 32 experts, [{rows} x {2 * I} x {H}], BF16 out")
+                                       shape=f"grouped {E} experts, [{rows} x {2 * I} x {H}], BF16 out")
         # fused SwiGLU -> 1x128 quantise of the gate/up output (the down projection's input)
         sq = torch.empty((rows, I), dtype=torch.uint8, device=dev)
         ss = torch.empty((I // 128, rows), dtype=torch.float32, device=dev)
@@ -392,7 +393,7 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
         ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm(aq, sa, rows, offsets, E, bq, sb, y2, fp8bs.OUT_BF16, H, I,
                                                        stream), stream, warmup, reps)
         out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
-                                    shape=f"grouped 32 experts, [{rows} x {H} x {I}], BF16 out")
+                                    shape=f"grouped {E} experts, [{rows} x {H} x {I}], BF16 out")
         del aq, sa, bq, sb, y2, d_in, w_dn
     if fp8bs.fp8bs_get_device_status(stream) != 0:
         raise RuntimeError("device status after the workload measurements")
@@ -413,6 +414,10 @@ def main():
                     help="comma-separated sections of the per-kernel lines to run: " + ", ".join(WORKLOAD_SECTIONS)
                          + " (wgrad also times the dual, power-of-two and re-tiling quantisations of its X; "
                            "moe the grouped GEMMs and the fused SwiGLU quantisation)")
+    ap.add_argument("--moe-tokens", type=int, default=8192,
+                    help="tokens of the MoE workload (8192: the benchmark's; smaller for profiling captures)")
+    ap.add_argument("--moe-experts", type=int, default=32,
+                    help="experts of the MoE workload (32: the benchmark's; top-8 routing needs at least 8)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -577,8 +582,10 @@ def main():
         unknown = set(sections) - set(WORKLOAD_SECTIONS)
         if unknown:
             raise SystemExit(f"unknown workload sections: {sorted(unknown)}")
+        if args.moe_experts < 8 or args.moe_tokens < 1:
+            raise SystemExit("--moe-experts must be at least 8 (top-8 routing) and --moe-tokens positive")
         workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup,
-                                      sections)
+                                      sections, args.moe_tokens, args.moe_experts)
     gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
     value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
