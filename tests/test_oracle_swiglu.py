@@ -73,3 +73,26 @@ def test_bf16_rounding_vs_brute_force():
     got = oracle.bf16_round_f64(np.array(vals))
     for v, g in zip(vals, got):
         assert float(g) == _bf16_brute(float(v)), v
+
+
+def test_swiglu_quantize_pipeline_by_hand():
+    """The composed oracle (SwiGLU -> BF16 -> 1x128 quantise) on rows worked
+    by hand: gate 30 and up 0.5 give v = 30 / (1 + e^-30) * 0.5, which rounds
+    to 15 in BF16 (e^-30 is far below half a BF16 ulp of 1), so the group's
+    scale is fl32(15 / 448) and every code is +448 (0x7E); negating up flips
+    every code to 0xFE; a zero gate row gives scale 0 and zero codes; and
+    swapping the gate and up halves (silu(0.5) * 30 = 9.34...) would change
+    the scale."""
+    inter = 128
+    h = np.zeros((3, 2 * inter), np.float32)
+    h[0, :inter], h[0, inter:] = 30.0, 0.5
+    h[1, :inter], h[1, inter:] = 30.0, -0.5
+    h[2, :inter], h[2, inter:] = 0.0, 7.0
+    q, s = oracle.swiglu_quantize_1x128(synth.f32_to_bf16_bits(h), inter)
+    assert s.shape == (3, 1) and q.shape == (3, inter)
+    assert s[0, 0] == np.float32(15.0) / np.float32(448.0)
+    assert s[1, 0] == s[0, 0]
+    assert np.all(q[0] == 0x7E) and np.all(q[1] == 0xFE)
+    assert s[2, 0] == 0 and np.all(q[2] == 0)
+    swapped = np.float32(0.5 / (1.0 + np.exp(-0.5)) * 30.0)
+    assert s[0, 0] != np.float32(swapped) / np.float32(448.0)
