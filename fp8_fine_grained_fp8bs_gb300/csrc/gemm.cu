@@ -52,15 +52,15 @@ constexpr int kBlockM = 128;
 constexpr int kBlockK = 128;         // = N_C
 constexpr int kUmmaK = 32;           // K of one kind::f8f6f4 MMA (bytes of E4M3)
 constexpr int kMaxGroups = 512;
-// Scale ring: kScaleSlots k-blocks of scales, handed between the loader
-// and the epilogue in chunks of kScaleChunk slots.  Every mbarrier
-// operation costs the epilogue warps a shared-memory round trip of some
-// 170 cycles while TMA and the tensor core keep shared memory busy, and
-// each epilogue warp handles every k-block, so the hand-off is per chunk
-// rather than per k-block.
-constexpr int kScaleChunk = 8;
+// Scale ring: Cfg::kScaleSlots k-blocks of scales, handed between the
+// loader and the epilogue in kScaleChunks chunks of Cfg::kScaleChunk slots.
+// Every mbarrier operation costs the epilogue warps a shared-memory round
+// trip of some 170 cycles while TMA and the tensor core keep shared memory
+// busy, and each epilogue warp handles every k-block, so the hand-off is
+// per chunk rather than per k-block: 16 k-blocks per chunk where the slots
+// are small (block-scaled B), 8 for row-scaled B, whose per-column slots
+// would otherwise crowd out operand stages.
 constexpr int kScaleChunks = 2;
-constexpr int kScaleSlots = kScaleChunk * kScaleChunks;
 constexpr uint32_t kTmemCols = 512;  // all of TMEM: 512 / BN partial buffers
 // Register split (setmaxnreg): the four producer/issuer warps shrink to
 // kRegsProducer, the eight epilogue warps grow to kRegsEpilogue, which holds
@@ -92,6 +92,8 @@ struct Cfg {
   // scale slot: A row scales, then B scales (per column, or one per
   // 128-column block padded to 16 bytes)
   static constexpr int kSlotFloats = kBlockM + (kRowScale ? BN : 4);
+  static constexpr int kScaleChunk = kRowScale ? 8 : 16;
+  static constexpr int kScaleSlots = kScaleChunk * kScaleChunks;
   static constexpr int kColsPerThread = BN / 2;
   static constexpr int kChunks = kColsPerThread / 32;
   static constexpr int kOutBytes = (kEpiThreads / 32) * kOutSlots * kOutBoxBytes;
@@ -479,13 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         const bool last_tile = t + nunits >= total_tiles;
         for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, ++step, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
-          const uint32_t chunk = (step / kScaleChunk) % kScaleChunks;
-          if (step % kScaleChunk == 0 &&
-              !mbar_wait(&sc_empty[chunk], ((step / kScaleSlots) & 1u) ^ 1u, p.timeout_ns)) {
+          const uint32_t chunk = (step / C::kScaleChunk) % kScaleChunks;
+          if (step % C::kScaleChunk == 0 &&
+              !mbar_wait(&sc_empty[chunk], ((step / C::kScaleSlots) & 1u) ^ 1u, p.timeout_ns)) {
             live = false;
             break;
           }
-          float* dst = sScale + (step % kScaleSlots) * C::kSlotFloats;
+          float* dst = sScale + (step % C::kScaleSlots) * C::kSlotFloats;
           const float* sa_kb = p.sa + static_cast<int64_t>(kb) * p.M;
 #pragma unroll
           for (int i = 0; i < kBlockM / 32; ++i) {
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nb = static_cast<int64_t>(g) * nnb + n0 / 128 + lane;
             cp_async_4(dst + kBlockM + lane, p.sb + nb * p.nkb + kb);
           }
-          if (step % kScaleChunk == kScaleChunk - 1 || (last_tile && kk + 1 == p.nkb))
+          if (step % C::kScaleChunk == C::kScaleChunk - 1 || (last_tile && kk + 1 == p.nkb))
             cp_async_mbar_arrive(&sc_full[chunk]);
         }
       }
@@ -537,15 +539,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C::kColsPerThread / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
       for (int kk = 0; kk < p.nkb; ++kk, ++step) {
-        const uint32_t chunk = (step / kScaleChunk) % kScaleChunks;
-        if (step % kScaleChunk == 0 &&
-            !mbar_wait(&sc_full[chunk], (step / kScaleSlots) & 1u, p.timeout_ns)) {
+        const uint32_t chunk = (step / C::kScaleChunk) % kScaleChunks;
+        if (step % C::kScaleChunk == 0 &&
+            !mbar_wait(&sc_full[chunk], (step / C::kScaleSlots) & 1u, p.timeout_ns)) {
           live = false;
           break;
         }
         if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
         tc_fence_after_sync();
-        const float* scs = sScale + (step % kScaleSlots) * C::kSlotFloats;
+        const float* scs = sScale + (step % C::kScaleSlots) * C::kSlotFloats;
         const float sa = scs[row_in_tile];
         const float s_ab = kRowScale ? sa : sa * scs[kBlockM + bsel];
         const float* scol = scs + kBlockM + colhalf * C::kColsPerThread;
@@ -578,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fold_block(acc2 + (ch + 1) * 16, rb, s_ab);
           }
         }
-        if (step % kScaleChunk == kScaleChunk - 1) {
+        if (step % C::kScaleChunk == C::kScaleChunk - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&sc_empty[chunk]);
         }
