@@ -420,6 +420,12 @@ def main():
                     help="experts of the MoE workload (32: the benchmark's; top-8 routing needs at least 8)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.sections = tuple(w for w in args.workloads.split(",") if w)
+    unknown = set(args.sections) - set(WORKLOAD_SECTIONS)
+    if unknown:
+        ap.error(f"unknown workload sections: {sorted(unknown)}")
+    if args.moe_experts < 8 or args.moe_tokens < 1:
+        ap.error("--moe-experts must be at least 8 (top-8 routing) and --moe-tokens positive")
     if args.impl == "reference":
         return run_reference(args)
 
@@ -578,14 +584,8 @@ def main():
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     workloads = None
     if not args.no_workloads:
-        sections = tuple(w for w in args.workloads.split(",") if w)
-        unknown = set(sections) - set(WORKLOAD_SECTIONS)
-        if unknown:
-            raise SystemExit(f"unknown workload sections: {sorted(unknown)}")
-        if args.moe_experts < 8 or args.moe_tokens < 1:
-            raise SystemExit("--moe-experts must be at least 8 (top-8 routing) and --moe-tokens positive")
         workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup,
-                                      sections, args.moe_tokens, args.moe_experts)
+                                      args.sections, args.moe_tokens, args.moe_experts)
     gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
     value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
