@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
 // and up, the next ones in flight); the 16 lanes of a half-warp are one
 // 1x128 group.  v = BF16_rne(silu(g) * u), silu(g) = g / (1 + exp(-g)) in
 // FP32 (hardware base-2 exponential and reciprocal: relative error below
-// 2^-16 for |g| <= 80), then the group is quantised exactly as
+// 2^-16 for every gate), then the group is quantised exactly as
 // fp8bs_quantize_act does with a BF16 input.
 constexpr int kSgThreads = 256;
 
@@ -857,19 +857,50 @@ __device__ __forceinline__ float rcp_ftz(float x) {
   return y;
 }
 
+// Gates below this take swiglu_far_negative: there 1 + e^-g exceeds 2^92 and,
+// from about -87.3 on, its one-instruction reciprocal would flush to zero
+// although silu(g) * u is still a normal number.
+constexpr float kFarNegativeGate = -64.0f;
+
+// silu(g) * u for g < -64, where silu(g) = g e^g / (1 + e^g) and e^g < 2^-92,
+// so silu(g) * u = g u e^g to well within 2^-24.  Evaluated without overflow
+// or flushing: with g = mg 2^eg and u = mu 2^eu (frexp, exact),
+// g log2(e) = n + f split by a two-part constant (log2 e = kHi + kLo, kHi with
+// 15 significant bits so that g * kHi is exact for a BF16 g, n = rint of it,
+// f in about [-0.5, 0.5]), the result is ldexp(mg mu 2^f, eg + eu + n): one
+// rounding in mg mu 2^f (mg mu is exact), ex2's error, and ldexp's exact
+// scaling (or its one rounding into the subnormal range).  Relative error
+// about 2^-21.  Below g = -200 the value is under 2^-152 for every finite
+// BF16 u, so it is a signed zero.  Not inlined: it runs only for such gates.
+__device__ __noinline__ float swiglu_far_negative(float g, float u) {
+  constexpr float kLog2eHi = 1.44268798828125f;   // 23637 / 16384
+  constexpr float kLog2eLo = 7.0526077e-06f;      // log2(e) - kLog2eHi, rounded to float32
+  if (g < -200.0f) return -copysignf(0.0f, u);    // the sign of g * u (g < 0)
+  int eg, eu;
+  const float mg = frexpf(g, &eg);
+  const float mu = frexpf(u, &eu);
+  const float th = g * kLog2eHi;                   // exact
+  const float n = rintf(th);
+  const float f = __fadd_rn(th - n, g * kLog2eLo); // th - n exact
+  return ldexpf(mg * mu * ex2_ftz(f), eg + eu + static_cast<int>(n));
+}
+
 // Two outputs v = BF16(silu(g) * u), silu(g) = g / (1 + e^-g) with
 // e^-g = 2^(-g log2 e); the multiplies and the add run as packed FP32x2
-// operations.  Relative error of silu below 2^-17 for |g| <= 80 (the
-// rounding of -g log2 e dominates: |g| log2(e) 2^-24 in the exponent).
-// Flushing subnormals changes nothing that matters: a subnormal e^-g only
-// adds to 1, a subnormal g gives 2^0 = 1, and 1/inf = 0 as before.
+// operations.  Relative error below 2^-16 for every gate: the rounding of
+// -g log2 e dominates (|g| log2(e) 2^-24 in the exponent, g >= -64 here) and
+// gates below -64 take swiglu_far_negative.  Flushing subnormals in ex2 and
+// rcp changes nothing that matters: a subnormal e^-g only adds to 1, a
+// subnormal g gives 2^0 = 1, and 1/inf = 0 as before.
 __device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw) {
   constexpr float kLog2e = 1.4426950408889634f;
   const float2 g = make_float2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
   const float2 u = make_float2(__uint_as_float(uw << 16), __uint_as_float(uw & 0xFFFF0000u));
   const float2 t = __fmul2_rn(g, make_float2(-kLog2e, -kLog2e));
   const float2 d = __fadd2_rn(make_float2(ex2_ftz(t.x), ex2_ftz(t.y)), make_float2(1.0f, 1.0f));
-  const float2 v = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
+  float2 v = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
+  if (g.x < kFarNegativeGate) v.x = swiglu_far_negative(g.x, u.x);
+  if (g.y < kFarNegativeGate) v.y = swiglu_far_negative(g.y, u.y);
   const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);  // v.x in the low half
   return *reinterpret_cast<const uint32_t*>(&b);
 }

@@ -181,7 +181,8 @@ int fp8bs_requant_1x128_to_128x1(const uint8_t* xq, const float* sx, int64_t M, 
  *   h   [M][ldh] BF16: the gate/up projection output, gate in columns [0, I),
  *       up in columns [I, 2I).                                        (in)
  *   q   [M][I] E4M3 codes.  s [I/128][M] float32, kb-major.            (out)
- * silu is evaluated in FP32 with a relative error below 2^-16 for |gate| <= 80,
+ * silu(gate) * up is evaluated in FP32 with a relative error below 2^-16 for
+ * every gate (gates below -64 take an overflow-free form g * up * e^g),
  * so a value within that distance of a BF16 rounding boundary may round either
  * way; codes and scales are otherwise those of quantising the rounded v.
  * Rules: I % 128 == 0, ldh >= 2*I, ldh*2 % 16 == 0; pointers 16-byte aligned.

@@ -19,10 +19,16 @@ import oracle
 F32_REL = 1e-5
 
 
+BF16_MIN_SUBNORMAL = 2.0 ** -133
+
+
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of the BF16 grid at v: 2^(e - 7) for |v| in [2^e, 2^(e+1)),
+    never below the subnormal spacing 2^-133 (which is also the ulp of 0)."""
     a = np.abs(np.asarray(v, dtype=np.float64))
     _, ex = np.frexp(np.where(a > 0, a, 1.0))
-    return np.exp2((ex.astype(np.int64) - 1 - 7).astype(np.float64))
+    ulp = np.exp2((ex.astype(np.int64) - 1 - 7).astype(np.float64))
+    return np.where(a > 0, np.maximum(ulp, BF16_MIN_SUBNORMAL), BF16_MIN_SUBNORMAL)
 
 
 def check_f32(gpu, Y, T, what=""):

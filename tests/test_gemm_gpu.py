@@ -202,6 +202,27 @@ def test_dense_fprop_full_size_sampled():
     print(f"elements accepted through the cancellation branch: {n_cancel}")
 
 
+@pytest.mark.slow
+def test_dense_fprop_full_output():
+    """Every element of Y[4096,7168] (BF16 out) against the oracle, as
+    benchmarked: the whole output, not samples.  The oracle runs over row
+    chunks of 512 to bound host memory (about 40 s of host time)."""
+    torch, fp8bs = require_gpu()
+    x_bits, w_bits = synth.dense_fprop(0)
+    xq, sx = fp8bs.quantize_act(to_dev_bf16(x_bits))
+    wq, sw = fp8bs.quantize_weight(to_dev_bf16(w_bits))
+    y = to_host(fp8bs.gemm(xq, sx, wq, sw, out_dtype=torch.bfloat16))
+    assert fp8bs.fp8bs_get_device_status() == 0
+    qa, sa = oracle.quantize_act_1x128(x_bits)
+    qb, sb = oracle.quantize_weight_128x128(w_bits)
+    n_cancel = 0
+    for r0 in range(0, x_bits.shape[0], 512):
+        rs = slice(r0, r0 + 512)
+        Y, T = oracle.gemm_block_scaled(qa[rs], sa[rs], qb, sb)
+        n_cancel += check_bf16(y[rs], Y, T, f"dense fprop rows {r0}..{r0 + 511}")
+    print(f"elements accepted through the cancellation branch: {n_cancel}")
+
+
 def test_bad_arguments_raise():
     torch, fp8bs = require_gpu()
     a = torch.zeros((128, 200), dtype=torch.uint8, device="cuda:0")

@@ -126,6 +126,13 @@ def test_moe_full_workload_sampled():
             check_bf16(got, Y, T, f"moe expert {g}")
         pad = torch.as_tensor(np.nonzero(src < 0)[0], device=y.device)
         assert int(torch.count_nonzero(y[pad])) == 0
+        # one whole expert, every row (padding included) and every column: the
+        # last expert, the smallest under the Zipf routing
+        lo, hi = int(offsets[G - 1]), int(offsets[G])
+        qa, sa = oracle.quantize_act_1x128(a_bits[lo:hi])
+        qb, sb = oracle.quantize_weight_128x128(w_bits[G - 1])
+        Y, T = oracle.gemm_block_scaled(qa, sa, qb, sb)
+        check_bf16(to_host(y[lo:hi]), Y, T, f"moe expert {G - 1}, whole segment [{lo}, {hi}) x {N}")
 
 
 def test_grouped_with_power_of_two_activation_scales():

@@ -2,8 +2,8 @@
 
 The reference is the unfused pipeline (DeepSeek-V3 §3.3.3 "low-precision
 activations" (2)): v = BF16(silu(gate) * up), then the 1x128 quantisation of
-v.  The kernel evaluates silu in FP32 with a relative error below 2^-16
-(|gate| <= 80), so where the exact value lies within that distance of a BF16
+v.  The kernel evaluates silu(gate) * up in FP32 with a relative error below
+2^-16 for every gate, so where the exact value lies within that distance of a BF16
 rounding boundary both neighbouring BF16 values are correct.  The check:
 
   * every group whose 128 values are unambiguous: codes and scale bit-exact
@@ -50,7 +50,11 @@ def _check(h_bits, inter, q_gpu, s_gpu, pow2):
     for m, g in zip(*np.nonzero(~clean)):
         a_lo = np.abs(lo3[m, g]).astype(np.float64)
         a_hi = np.abs(hi3[m, g]).astype(np.float64)
-        choices = {float(np.maximum(a_lo, a_hi).max()), float(np.minimum(a_lo, a_hi).max())}
+        small, large = np.minimum(a_lo, a_hi), np.maximum(a_lo, a_hi)
+        # every absmax some choice of roundings attains: a candidate magnitude
+        # of some element that is at least every element's smaller candidate
+        floor = small.max()
+        choices = {float(a) for a in np.concatenate([small, large]) if a >= floor}
         s = np.float32(s_gpu[m, g])
         ok_scales = {float(_scale(np.float32(a), pow2)) for a in choices}
         assert float(s) in ok_scales, (m, g, float(s), ok_scales)
@@ -83,7 +87,8 @@ def test_swiglu_quantize(M, I, pow2):
 
 
 def test_swiglu_quantize_edge_values():
-    """Zero rows, +-0, large |gate| (silu -> g and -> 0), tiny products."""
+    """Zero rows, +-0, large |gate| (silu -> g and -> 0), tiny products, and
+    gates from -64 down to -300 with up values up to 3e38."""
     I = 256
     h = synth.normal_bf16((16, 2 * I), 1.7, 61, 5).view(np.uint16).copy()
     f = oracle.bf16_bits_to_f32(h).copy()
@@ -94,6 +99,17 @@ def test_swiglu_quantize_edge_values():
     f[3, I:] = np.linspace(-3, 3, I, dtype=np.float32)
     f[4, I:] = 1e-30
     f[5, :I] = -40.0
+    # gates far below zero: silu(g) * u = g u e^g stays a normal number where
+    # 1 + e^-g is beyond the one-instruction reciprocal's range
+    f[6, :I] = np.linspace(-100, -80, I, dtype=np.float32)
+    f[6, I:] = 1e30
+    f[7, :I] = np.linspace(-200, -64, I, dtype=np.float32)
+    f[7, I:] = 1e35
+    f[8, :I] = np.repeat(np.float32([-87.5, -88.0, -90.0, -95.0]), I // 4)    # ordinary up values
+    f[9, :I] = np.linspace(-300, -150, I, dtype=np.float32)
+    f[9, I:] = 3e38
+    f[10, :I] = -64.5
+    f[10, I:] = np.linspace(-2e27, 2e27, I, dtype=np.float32)
     h = synth.f32_to_bf16_bits(f)
     for pow2 in (False, True):
         q, s = _run(h, I, pow2)
