@@ -55,6 +55,14 @@ WORKLOAD = ("dense fprop: quantize X[4096,7168] 1x128 + W[7168,7168] 128x128 to 
             "block-scaled FP8 GEMM Y=X W^T BF16 out; plus standalone quantize of X[16384,7168]")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0      # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL_HBM_GBS = 7900.0 # HBM3e of one GB300, nominal
+FP8_FLOP_PER_CLK_SM = 16384  # dense FP8 tcgen05 rate per SM (M=128 x N=256 x K=32 MMA in 128 cycles)
+
+
+def hw_fp8_peak_tflops(sms: int, sm_mhz: float) -> float:
+    """Instruction-rate FP8 peak: every SM issuing dense FP8 MMAs at its full
+    rate at the given clock."""
+    return sms * FP8_FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
 
 
 def _peaks():
@@ -154,8 +162,51 @@ def _cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(x_bits, w_bits, budget_s=12.0):
-    """The oracle, untuned, on a bounded sample: X rows x W rows of the step."""
+def _oracle_quantize_rows(rows_bits) -> int:
+    """The oracle's 1x128 quantisation of a block of rows; returns the element count."""
+    import oracle
+    oracle.quantize_act_1x128(rows_bits)
+    return int(rows_bits.size)
+
+
+def cpu_quantize_baseline(xl_bits, budget_s: float = 4.0):
+    """The oracle's 1x128 quantisation of X[16384,7168], untuned, on bounded
+    samples: on one core (the numpy oracle is single-threaded elementwise
+    code) and on all cores (one 256-row shard per core, a process pool
+    started with spawn, so no process is forked after the GPU is in use)."""
+    import multiprocessing
+    rows = 256
+    bpe = 2 + 1 + 4 / 128
+    nrows = xl_bits.shape[0]
+    el, n, t0 = 0, 0, time.perf_counter()
+    while True:
+        r0 = (n * rows) % (nrows - rows)
+        el += _oracle_quantize_rows(xl_bits[r0:r0 + rows])
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    one = el * bpe / (time.perf_counter() - t0) / 1e9
+    cores = os.cpu_count() or 1
+    shards = [np.ascontiguousarray(xl_bits[(i * rows) % nrows:(i * rows) % nrows + rows]) for i in range(cores)]
+    with multiprocessing.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_quantize_rows, shards)            # start-up and imports, untimed
+        el_all, reps, t0 = 0, 0, time.perf_counter()
+        while True:
+            el_all += sum(pool.map(_oracle_quantize_rows, shards))
+            reps += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt_all = time.perf_counter() - t0
+    return {"unit": "GB/s", "one_core": one, "all_cores": el_all * bpe / dt_all / 1e9, "cores": cores,
+            "kind": "oracle",
+            "sample": f"one core: {n} blocks of 256 rows of X[16384,7168]; all cores: {reps} rounds of "
+                      f"{cores} such blocks, one per process; algorithmic bytes 2 + 1 + 4/128 per element"}
+
+
+def cpu_baseline(x_bits, w_bits, xl_bits=None, budget_s=12.0):
+    """The oracle, untuned, on a bounded sample: X rows x W rows of the step;
+    with xl_bits also the standalone 1x128 quantisation (one core and all
+    cores)."""
     sm_rows, sn_rows = 512, 1024
     flop, t0, n = 0.0, time.perf_counter(), 0
     while True:
@@ -164,9 +215,12 @@ def cpu_baseline(x_bits, w_bits, budget_s=12.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
-            "sample": f"{n} x (quantize X[{sm_rows},7168] 1x128 + W[{sn_rows},7168] 128x128, "
-                      f"GEMM {sm_rows}x{sn_rows}x7168), float64 numpy, {dt:.1f} s"}
+    out = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
+           "sample": f"{n} x (quantize X[{sm_rows},7168] 1x128 + W[{sn_rows},7168] 128x128, "
+                     f"GEMM {sm_rows}x{sn_rows}x7168), float64 numpy, {dt:.1f} s"}
+    if xl_bits is not None:
+        out["quantize_1x128"] = cpu_quantize_baseline(xl_bits)
+    return out
 
 
 def run_reference(args):
@@ -221,11 +275,12 @@ def _time_ms(fn, stream, warmup: int, reps: int) -> float:
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-WORKLOAD_SECTIONS = ("dgrad", "wgrad", "context", "weight", "moe")
+WORKLOAD_SECTIONS = ("dgrad", "wgrad", "context", "weight", "moe", "pow2")
 
 
 def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm_peak: float, warmup: int,
-                      sections=WORKLOAD_SECTIONS, moe_tokens: int = 8192, moe_experts: int = 32):
+                      sections=WORKLOAD_SECTIONS, moe_tokens: int = 8192, moe_experts: int = 32,
+                      hw_peak: float | None = None):
     """The other configurations of the path, each kernel timed alone.
 
     * MoE grouped fprop: 8192 tokens, top-8 of 32 experts (Zipf s=1.1),
@@ -248,11 +303,15 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
 
     def gemm_line(flop, ms, **extra):
         tf = flop / (ms * 1e-3) / 1e12
-        return {"tflops": tf, "ms": ms, "frac_of_fp8_peak": tf / fp8_peak, "gflop": flop / 1e9, **extra}
+        line = {"tflops": tf, "ms": ms, "frac_of_fp8_peak": tf / fp8_peak, "gflop": flop / 1e9, **extra}
+        if hw_peak:
+            line["frac_of_hw_rate"] = tf / hw_peak
+        return line
 
     def bw_line(nbytes, ms, **extra):
         gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"gbs": gbs, "ms": ms, "frac_of_hbm": gbs / hbm_peak, "bytes": nbytes, **extra}
+        return {"gbs": gbs, "ms": ms, "frac_of_hbm": gbs / hbm_peak, "frac_of_nominal_hbm": gbs / NOMINAL_HBM_GBS,
+                "bytes": nbytes, **extra}
 
     if "dgrad" in sections:
         # ---- dgrad
@@ -395,6 +454,74 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
         out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
                                     shape=f"grouped {E} experts, [{rows} x {H} x {I}], BF16 out")
         del aq, sa, bq, sb, y2, d_in, w_dn
+    if "pow2" in sections:
+        # ---- power-of-two scales applied by the tensor core (UE8M0 block
+        # scales of tcgen05.mma.kind::mxf8f6f4), next to the fold GEMM on the
+        # same operands: the dense fprop shape, the MoE expert GEMMs and Wgrad
+        x_bits, w_bits = synth.dense_fprop(seed=rank)
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        w = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        xq, sx = fp8bs.quantize_act(x, pow2=True)
+        wq, sw = fp8bs.quantize_weight(w, pow2=True)
+        yp = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+        flop = 2.0 * 4096 * 7168 * 7168
+        ms = _time_ms(lambda: fp8bs.fp8bs_gemm_pow2(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, yp, fp8bs.OUT_BF16,
+                                                    4096, 7168, 7168, 0, stream), stream, warmup, reps)
+        out["gemm_pow2_dense"] = gemm_line(flop, ms, shape="M=4096 N=7168 K=7168, power-of-two scales in the MMA "
+                                                            "(kind::mxf8f6f4, UE8M0), BF16 out")
+        ms = _time_ms(lambda: fp8bs.fp8bs_gemm(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, yp, fp8bs.OUT_BF16,
+                                               4096, 7168, 7168, 0, stream), stream, warmup, reps)
+        out["gemm_fold_dense_same_operands"] = gemm_line(flop, ms, shape="the same power-of-two operands through "
+                                                                         "the CUDA-core fold GEMM")
+        del x, w, xq, sx, wq, sw, yp
+        # Wgrad: dY re-tiled 1x128 -> 128x1 from FP8 (power-of-two), X quantised 128x1
+        dy_bits, x_bits = synth.wgrad(seed=rank)
+        dy = torch.from_numpy(dy_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        dyq, sdy = fp8bs.quantize_act(dy, pow2=True)
+        dyq_t, sdy_t = fp8bs.requant_1x128_to_128x1(dyq, sdy, pow2=True)
+        _, _, xq_t, sx_t = fp8bs.quantize_act(x, transposed=True, pow2=True)
+        dw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_gemm_pow2(dyq_t, sdy_t, xq_t, sx_t, fp8bs.SCALE_ROW1x128, dw,
+                                                    fp8bs.OUT_F32, 2048, 7168, 16384, 0, stream), stream, warmup, reps)
+        out["wgrad_pow2"] = gemm_line(2.0 * 2048 * 7168 * 16384, ms,
+                                      shape="M=2048 N=7168 K=T=16384, row-scaled B, power-of-two scales in the MMA, "
+                                            "FP32 out")
+        del dy, x, dyq, sdy, dyq_t, sdy_t, xq_t, sx_t, dw
+        # MoE expert GEMMs with power-of-two activation and weight scales
+        E, H, I = moe_experts, 7168, 2048
+        choice = synth.moe_routing(seed=rank, tokens=moe_tokens, experts=E)
+        offsets_np, src_np = synth.moe_layout(choice, E)
+        rows = int(offsets_np[-1])
+        real_rows = int((src_np >= 0).sum())
+        offsets = torch.from_numpy(offsets_np).to(dev)
+        gp = torch.Generator(device=dev)
+        gp.manual_seed(3000 + rank)
+        ok = torch.from_numpy(src_np).to(dev) >= 0
+        a_in = torch.randn((rows, H), generator=gp, device=dev).to(torch.bfloat16)
+        a_in[~ok] = 0
+        w_gu = (torch.randn((E * 2 * I, H), generator=gp, device=dev) * 0.02).to(torch.bfloat16)
+        aq, sa = fp8bs.quantize_act(a_in, pow2=True)
+        bq, sb = fp8bs.quantize_weight(w_gu, pow2=True)
+        y1 = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm_pow2(aq, sa, rows, offsets, E, bq, sb, y1, fp8bs.OUT_BF16,
+                                                            2 * I, H, stream), stream, warmup, reps)
+        out["moe_gate_up_pow2"] = gemm_line(2.0 * real_rows * 2 * I * H, ms, rows=rows, real_rows=real_rows,
+                                            shape=f"grouped {E} experts, [{rows} x {2 * I} x {H}], power-of-two "
+                                                  f"scales in the MMA, BF16 out")
+        del a_in, w_gu, aq, sa, bq, sb, y1
+        d_in = torch.randn((rows, I), generator=gp, device=dev).to(torch.bfloat16)
+        d_in[~ok] = 0
+        w_dn = (torch.randn((E * H, I), generator=gp, device=dev) * 0.02).to(torch.bfloat16)
+        aq, sa = fp8bs.quantize_act(d_in, pow2=True)
+        bq, sb = fp8bs.quantize_weight(w_dn, pow2=True)
+        y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_grouped_gemm_pow2(aq, sa, rows, offsets, E, bq, sb, y2, fp8bs.OUT_BF16,
+                                                            H, I, stream), stream, warmup, reps)
+        out["moe_down_pow2"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
+                                         shape=f"grouped {E} experts, [{rows} x {H} x {I}], power-of-two scales in "
+                                               f"the MMA, BF16 out")
+        del d_in, w_dn, aq, sa, bq, sb, y2, ok
     if fp8bs.fp8bs_get_device_status(stream) != 0:
         raise RuntimeError("device status after the workload measurements")
     torch.cuda.empty_cache()
@@ -470,38 +597,54 @@ def main():
 
     # X (1x128) and W (128x128) are quantised by one launch whose persistent
     # grid walks X's tiles, then W's; then the GEMM.
-    def step(gemm_events=None):
+    def quantize_step():
         fp8bs.fp8bs_quantize_act_weight(xin, M, K, K, xq, sx, win, N, K, K, wq, sw, fp8bs.SCALE_ABSMAX, stream)
-        if gemm_events is not None:
-            gemm_events[0].record(stream)
+
+    def gemm_step():
         fp8bs.fp8bs_gemm(xq, sx, wq, sw, fp8bs.SCALE_BLOCK128x128, y, fp8bs.OUT_BF16, M, N, K, 0, stream)
-        if gemm_events is not None:
-            gemm_events[1].record(stream)
 
     for _ in range(args.warmup):
-        step()
+        quantize_step()
+        gemm_step()
     torch.cuda.synchronize(dev)
     if fp8bs.fp8bs_get_device_status(stream) != 0:
         raise RuntimeError("device status after warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # the steps: nothing recorded between the two launches of a step
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(_gpu_id(torch, local))
     sampler.start()
     barrier()
     torch.cuda.synchronize(dev)
     t_start.record(stream)
-    for i in range(args.steps):
-        step(ev[i])
+    for _ in range(args.steps):
+        quantize_step()
+        gemm_step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop()
     ms_step = max_over_ranks(t_start.elapsed_time(t_end) / args.steps)
-    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    gemm_ms = max_over_ranks(gemm_ms)
     if fp8bs.fp8bs_get_device_status(stream) != 0:
         raise RuntimeError("device status after the timed steps")
+
+    # the GEMM alone, on the operands the steps produced: CUDA events around
+    # each launch on the launching stream (the dominant kernel's roofline)
+    # (its operands, 80 MB, fit in L2: a 256 MB write before each launch,
+    # outside the timed pair, leaves them in HBM)
+    ng = max(10, min(args.steps, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ng)]
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        l2_flush.fill_(1)
+        a.record(stream)
+        gemm_step()
+        b.record(stream)
+    del l2_flush
+    torch.cuda.synchronize(dev)
+    gemm_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
 
     # standalone quantize of X[16384, 7168] (inputs 235 MB > L2)
     xl_bits = synth.quantize_input(seed=rank)
@@ -582,13 +725,19 @@ def main():
 
     peaks, peak_src = _peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    hw_peak = hw_fp8_peak_tflops(sms, max_mhz)
     workloads = None
     if not args.no_workloads:
         workloads = measure_workloads(fp8bs, synth, dev, stream, rank, fp8_peak, peaks["hbm_gbs"], args.warmup,
-                                      args.sections, args.moe_tokens, args.moe_experts)
+                                      args.sections, args.moe_tokens, args.moe_experts, hw_peak)
     gemm_tflops = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
     q_gbs = QUANT_BYTES / (q_ms * 1e-3) / 1e9
     value = world * GEMM_FLOP / (ms_step * 1e-3) / 1e12
+    # The contract keys first, then the per-configuration lines, and the
+    # dominant kernels' figures last (the end of the line is what a truncated
+    # log keeps).
     line = {
         "metric": METRIC,
         "value": value,
@@ -604,30 +753,35 @@ def main():
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "out": "bf16",
                    "quantize_shape": [QM, QK], "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (X+W BF16 = 161 MB per step > 129 MB); no flush"},
-        "gemm": {"tflops": gemm_tflops, "ms": gemm_ms, "frac_of_fp8_peak": gemm_tflops / fp8_peak},
-        "quantize": {"gbs": q_gbs, "ms": q_ms, "frac_of_hbm": q_gbs / peaks["hbm_gbs"],
-                     "bytes": QUANT_BYTES},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp8_peak,
-                     "traffic": _traffic("gemm_dense_fprop_bf16",
-                                         "fp8_fine_grained_fp8bs_gb300/csrc/gemm.cu"),
-                     "peak_source": f"{peak_src}: bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)"},
-        "quantize_roofline": {"bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                              "frac": q_gbs / peaks["hbm_gbs"],
-                              "traffic": _traffic("quantize_act_1x128_16384x7168",
-                                                  "fp8_fine_grained_fp8bs_gb300/csrc/quantize.cu"),
-                              "peak_source": peak_src},
+                   "l2": "steps: inputs larger than L2 (X+W BF16 = 161 MB per step > 129 MB), no flush; "
+                         "GEMM alone: 256 MB written before each timed launch (L2 flush)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
         "e2e": {"value": world * GEMM_FLOP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(xin.numel() * 2 + win.numel() * 2),
                 "d2h_bytes_per_step": int(y.numel() * 2), "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
-        "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x_bits, w_bits, xl_bits)
     if workloads is not None:
         line["workloads"] = workloads
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x_bits, w_bits)
+    line["roofline"] = {
+        "bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+        "frac": gemm_tflops / fp8_peak,
+        "traffic": _traffic("gemm_dense_fprop_bf16", "fp8_fine_grained_fp8bs_gb300/csrc/gemm.cu"),
+        "peak_source": f"{peak_src}: bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)",
+        "hw_rate_peak": hw_peak, "frac_of_hw_rate": gemm_tflops / hw_peak,
+        "hw_rate_source": f"{sms} SMs x 16384 FP8 FLOP/clk/SM x {max_mhz:g} MHz (maximum SM clock)"}
+    line["gemm"] = {"tflops": gemm_tflops, "ms": gemm_ms, "frac_of_fp8_peak": gemm_tflops / fp8_peak,
+                    "frac_of_hw_rate": gemm_tflops / hw_peak}
+    line["quantize_roofline"] = {
+        "bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": q_gbs / peaks["hbm_gbs"],
+        "traffic": _traffic("quantize_act_1x128_16384x7168", "fp8_fine_grained_fp8bs_gb300/csrc/quantize.cu"),
+        "peak_source": peak_src, "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS,
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS}
+    line["quantize"] = {"gbs": q_gbs, "ms": q_ms, "frac_of_hbm": q_gbs / peaks["hbm_gbs"],
+                        "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS, "bytes": QUANT_BYTES}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

@@ -22,6 +22,7 @@ from .build import LIB_PATH, build as _build
 __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
+    "fp8bs_gemm_pow2", "fp8bs_grouped_gemm_pow2",
     "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_quantize_act_weight", "quantize_act_weight", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string", "fp8bs_selftest_wait_timeout",
     "fp8bs_diag_gemm_unpromoted", "diag_gemm_unpromoted",
@@ -60,6 +61,9 @@ _SIGNATURES = {
     "fp8bs_gemm": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
     "fp8bs_grouped_gemm": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                            _c_vp],
+    "fp8bs_gemm_pow2": [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_vp],
+    "fp8bs_grouped_gemm_pow2": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
+                                _c_vp],
     "fp8bs_get_device_status": [_c_vp],
     "fp8bs_selftest_wait_timeout": [_c_i64, _c_vp],
     "fp8bs_diag_gemm_unpromoted": [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp],
@@ -162,6 +166,18 @@ def fp8bs_grouped_gemm(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N
                                   _ptr(d), d_dtype, N, K, _stream(stream)), "fp8bs_grouped_gemm")
 
 
+def fp8bs_gemm_pow2(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate=0, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_gemm_pow2(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), sb_kind, _ptr(d), d_dtype, M, N, K,
+                               int(accumulate), _stream(stream)), "fp8bs_gemm_pow2")
+
+
+def fp8bs_grouped_gemm_pow2(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N, K, stream=None):
+    lib = load_library()
+    _check(lib.fp8bs_grouped_gemm_pow2(_ptr(a), _ptr(sa), M_total, _ptr(offsets), num_groups, _ptr(b), _ptr(sb),
+                                       _ptr(d), d_dtype, N, K, _stream(stream)), "fp8bs_grouped_gemm_pow2")
+
+
 def fp8bs_get_device_status(stream=None) -> int:
     return load_library().fp8bs_get_device_status(_stream(stream))
 
@@ -248,27 +264,31 @@ def requant_1x128_to_128x1(xq, sx, pow2: bool = True, stream=None):
 
 
 def gemm(a, sa, b, sb, sb_kind: int = SCALE_BLOCK128x128, out_dtype=None, out=None, accumulate: bool = False,
-         stream=None):
-    """D = A B^T with per-128-K-block scales; A [M,K], B [N,K] uint8 E4M3."""
+         stream=None, pow2: bool = False):
+    """D = A B^T with per-128-K-block scales; A [M,K], B [N,K] uint8 E4M3.
+    ``pow2``: power-of-two scales applied by the tensor core (fp8bs_gemm_pow2)."""
     import torch
     M, K = a.shape
     N = b.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
     d_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
-    fp8bs_gemm(a, sa, b, sb, sb_kind, out, d_dtype, M, N, K, int(accumulate), stream)
+    fn = fp8bs_gemm_pow2 if pow2 else fp8bs_gemm
+    fn(a, sa, b, sb, sb_kind, out, d_dtype, M, N, K, int(accumulate), stream)
     return out
 
 
-def grouped_gemm(a, sa, offsets, b, sb, out_dtype=None, out=None, stream=None):
-    """Per-expert D rows = A rows of the expert x B[g]^T; offsets: int32 CUDA tensor [G+1]."""
+def grouped_gemm(a, sa, offsets, b, sb, out_dtype=None, out=None, stream=None, pow2: bool = False):
+    """Per-expert D rows = A rows of the expert x B[g]^T; offsets: int32 CUDA tensor [G+1].
+    ``pow2``: power-of-two scales applied by the tensor core (fp8bs_grouped_gemm_pow2)."""
     import torch
     M, K = a.shape
     G, N, _ = b.shape
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
     d_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
-    fp8bs_grouped_gemm(a, sa, M, offsets, G, b, sb, out, d_dtype, N, K, stream)
+    fn = fp8bs_grouped_gemm_pow2 if pow2 else fp8bs_grouped_gemm
+    fn(a, sa, M, offsets, G, b, sb, out, d_dtype, N, K, stream)
     return out
 
 

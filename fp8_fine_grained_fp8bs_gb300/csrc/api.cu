@@ -157,42 +157,54 @@ int fp8bs_swiglu_quantize(const void* h, int64_t M, int64_t I, int64_t ldh, uint
                                                  static_cast<cudaStream_t>(stream)));
 }
 
-static int run_gemm(const fp8bs::GemmArgs& args, void* stream) {
+static int run_gemm(const fp8bs::GemmArgs& args, bool pow2, void* stream) {
   int sms = 0;
   const int st = current_device(&sms);
   if (st != FP8BS_OK) return st;
   bool tmap_failed = false, reg_failed = false;
-  const cudaError_t e =
-      fp8bs::launch_gemm(args, sms, static_cast<cudaStream_t>(stream), &tmap_failed, &reg_failed);
+  const cudaError_t e = pow2 ? fp8bs::launch_gemm_pow2(args, sms, static_cast<cudaStream_t>(stream), &tmap_failed,
+                                                       &reg_failed)
+                             : fp8bs::launch_gemm(args, sms, static_cast<cudaStream_t>(stream), &tmap_failed,
+                                                  &reg_failed);
   if (tmap_failed) return FP8BS_ERR_ALIGNMENT;
   return from_cuda(e);
 }
 
-int fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int sb_kind, void* d,
-               int d_dtype, int64_t M, int64_t N, int64_t K, int accumulate, void* stream) {
+// Argument checks of fp8bs_gemm(_pow2); FP8BS_OK with *g filled, or an
+// error; *nothing is set when the call has no work (M or N zero).
+static int gemm_args(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int sb_kind, void* d,
+                     int d_dtype, int64_t M, int64_t N, int64_t K, int accumulate, fp8bs::GemmArgs* g,
+                     bool* nothing) {
+  *nothing = false;
   if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
   if (sb_kind != FP8BS_SCALE_BLOCK128x128 && sb_kind != FP8BS_SCALE_ROW1x128) return FP8BS_ERR_INVALID_ARG;
   if (d_dtype != FP8BS_OUT_F32 && d_dtype != FP8BS_OUT_BF16) return FP8BS_ERR_INVALID_ARG;
   if (accumulate && d_dtype != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0 || N % 128 != 0) return FP8BS_ERR_SHAPE;
   if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
-  if (M == 0 || N == 0) return FP8BS_OK;
+  if (M == 0 || N == 0) {
+    *nothing = true;
+    return FP8BS_OK;
+  }
   if (K == 0) return FP8BS_ERR_SHAPE;
   if (a == nullptr || sa == nullptr || b == nullptr || sb == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_ERR_ALIGNMENT;
   if (sb_kind == FP8BS_SCALE_ROW1x128 && !aligned16(sb)) return FP8BS_ERR_ALIGNMENT;
-  fp8bs::GemmArgs g{};
-  g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.d = d; g.offsets = nullptr;
-  g.M = M; g.N = N; g.K = K; g.num_groups = 1; g.grouped = false;
-  g.sb_row = sb_kind == FP8BS_SCALE_ROW1x128;
-  g.out_bf16 = d_dtype == FP8BS_OUT_BF16;
-  g.accumulate = accumulate != 0;
-  g.timeout_ns = g_timeout_ns.load();
-  return run_gemm(g, stream);
+  *g = fp8bs::GemmArgs{};
+  g->a = a; g->sa = sa; g->b = b; g->sb = sb; g->d = d; g->offsets = nullptr;
+  g->M = M; g->N = N; g->K = K; g->num_groups = 1; g->grouped = false;
+  g->sb_row = sb_kind == FP8BS_SCALE_ROW1x128;
+  g->out_bf16 = d_dtype == FP8BS_OUT_BF16;
+  g->accumulate = accumulate != 0;
+  g->timeout_ns = g_timeout_ns.load();
+  return FP8BS_OK;
 }
 
-int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets, int num_groups,
-                       const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N, int64_t K, void* stream) {
+// Argument checks of fp8bs_grouped_gemm(_pow2), as gemm_args.
+static int grouped_args(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets, int num_groups,
+                        const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N, int64_t K,
+                        fp8bs::GemmArgs* g, bool* nothing) {
+  *nothing = false;
   if (M_total < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
   if (num_groups < 1 || num_groups > 512) return FP8BS_ERR_INVALID_ARG;
   if (d_dtype != FP8BS_OUT_F32 && d_dtype != FP8BS_OUT_BF16) return FP8BS_ERR_INVALID_ARG;
@@ -200,18 +212,58 @@ int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const
   if (K % 128 != 0 || N % 128 != 0) return FP8BS_ERR_SHAPE;
   if (M_total > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 24) || K > (int64_t(1) << 24))
     return FP8BS_ERR_SHAPE;
-  if (M_total == 0 || N == 0) return FP8BS_OK;
+  if (M_total == 0 || N == 0) {
+    *nothing = true;
+    return FP8BS_OK;
+  }
   if (K == 0) return FP8BS_ERR_SHAPE;
   if (a == nullptr || sa == nullptr || b == nullptr || sb == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8BS_ERR_ALIGNMENT;
-  fp8bs::GemmArgs g{};
-  g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.d = d; g.offsets = offsets;
-  g.M = M_total; g.N = N; g.K = K; g.num_groups = num_groups; g.grouped = true;
-  g.sb_row = false;
-  g.out_bf16 = d_dtype == FP8BS_OUT_BF16;
-  g.accumulate = false;
-  g.timeout_ns = g_timeout_ns.load();
-  return run_gemm(g, stream);
+  *g = fp8bs::GemmArgs{};
+  g->a = a; g->sa = sa; g->b = b; g->sb = sb; g->d = d; g->offsets = offsets;
+  g->M = M_total; g->N = N; g->K = K; g->num_groups = num_groups; g->grouped = true;
+  g->sb_row = false;
+  g->out_bf16 = d_dtype == FP8BS_OUT_BF16;
+  g->accumulate = false;
+  g->timeout_ns = g_timeout_ns.load();
+  return FP8BS_OK;
+}
+
+int fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int sb_kind, void* d,
+               int d_dtype, int64_t M, int64_t N, int64_t K, int accumulate, void* stream) {
+  fp8bs::GemmArgs g;
+  bool nothing = false;
+  const int st = gemm_args(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate, &g, &nothing);
+  if (st != FP8BS_OK || nothing) return st;
+  return run_gemm(g, false, stream);
+}
+
+int fp8bs_gemm_pow2(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int sb_kind, void* d,
+                    int d_dtype, int64_t M, int64_t N, int64_t K, int accumulate, void* stream) {
+  fp8bs::GemmArgs g;
+  bool nothing = false;
+  const int st = gemm_args(a, sa, b, sb, sb_kind, d, d_dtype, M, N, K, accumulate, &g, &nothing);
+  if (st != FP8BS_OK || nothing) return st;
+  return run_gemm(g, true, stream);
+}
+
+int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets, int num_groups,
+                       const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N, int64_t K, void* stream) {
+  fp8bs::GemmArgs g;
+  bool nothing = false;
+  const int st = grouped_args(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N, K, &g, &nothing);
+  if (st != FP8BS_OK || nothing) return st;
+  return run_gemm(g, false, stream);
+}
+
+int fp8bs_grouped_gemm_pow2(const uint8_t* a, const float* sa, int64_t M_total, const int32_t* offsets,
+                            int num_groups, const uint8_t* b, const float* sb, void* d, int d_dtype, int64_t N,
+                            int64_t K, void* stream) {
+  fp8bs::GemmArgs g;
+  bool nothing = false;
+  const int st = grouped_args(a, sa, M_total, offsets, num_groups, b, sb, d, d_dtype, N, K, &g, &nothing);
+  if (st != FP8BS_OK || nothing) return st;
+  return run_gemm(g, true, stream);
 }
 
 int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream) {
@@ -241,11 +293,12 @@ int fp8bs_diag_gemm_unpromoted(const uint8_t* a, const uint8_t* b, float* d, int
 
 int fp8bs_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-  int v = 0, q = 0, dg = 0;
+  int v = 0, mx = 0, q = 0, dg = 0;
   if (fp8bs::gemm_take_status(&v) != cudaSuccess) return FP8BS_ERR_CUDA;
+  if (fp8bs::gemm_mx_take_status(&mx) != cudaSuccess) return FP8BS_ERR_CUDA;
   if (fp8bs::quant_take_status(&q) != cudaSuccess) return FP8BS_ERR_CUDA;
   if (fp8bs::diag_take_status(&dg) != cudaSuccess) return FP8BS_ERR_CUDA;
-  return v != FP8BS_OK ? v : q != FP8BS_OK ? q : dg;
+  return v != FP8BS_OK ? v : mx != FP8BS_OK ? mx : q != FP8BS_OK ? q : dg;
 }
 
 int fp8bs_set_wait_timeout_ms(int64_t ms) {

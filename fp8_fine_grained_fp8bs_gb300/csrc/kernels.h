@@ -65,6 +65,15 @@ cudaError_t launch_gemm(const GemmArgs& args, int sm_count, cudaStream_t stream,
 // copy on the current device.
 cudaError_t gemm_take_status(int* status);
 
+// ---- gemm_mx.cu
+// The same GEMM for power-of-two scales, with the scales applied by the
+// tensor core (tcgen05.mma.kind::mxf8f6f4.block_scale, UE8M0) and all of K
+// accumulated in tensor memory.  A scale that is not zero or a power of two
+// in [2^-127, 2^127] records FP8BS_ERR_DEVICE_ARG in its status word.
+cudaError_t launch_gemm_pow2(const GemmArgs& args, int sm_count, cudaStream_t stream, bool* tmap_failed,
+                             bool* reg_check_failed);
+cudaError_t gemm_mx_take_status(int* status);
+
 // Diagnostic: a kernel whose bounded wait runs out (nothing ever arrives on
 // its barrier) and records FP8BS_ERR_TIMEOUT in the GEMM status word.
 cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, cudaStream_t stream);

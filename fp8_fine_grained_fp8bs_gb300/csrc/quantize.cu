@@ -857,10 +857,19 @@ __device__ __forceinline__ float rcp_ftz(float x) {
   return y;
 }
 
-// Gates below this take swiglu_far_negative: there 1 + e^-g exceeds 2^92 and,
+// Gates below -64 take swiglu_far_negative: there 1 + e^-g exceeds 2^92 and,
 // from about -87.3 on, its one-instruction reciprocal would flush to zero
-// although silu(g) * u is still a normal number.
-constexpr float kFarNegativeGate = -64.0f;
+// although silu(g) * u is still a normal number.  As BF16 bit patterns these
+// gates are exactly the patterns above 0xC280 (-64.0; NaNs are outside the
+// contract).
+constexpr uint32_t kFarNegativeBits = 0xC280u;
+
+// Whether any of the 8 BF16 gates in g lies below -64: the largest of the
+// 16-bit patterns, three two-lane maxima and one of the halves.
+__device__ __forceinline__ bool any_far_negative(const uint4& g) {
+  const uint32_t m = umax16x2(umax16x2(g.x, g.y), umax16x2(g.z, g.w));
+  return max(m & 0xFFFFu, m >> 16) > kFarNegativeBits;
+}
 
 // silu(g) * u for g < -64, where silu(g) = g e^g / (1 + e^g) and e^g < 2^-92,
 // so silu(g) * u = g u e^g to well within 2^-24.  Evaluated without overflow
@@ -871,8 +880,8 @@ constexpr float kFarNegativeGate = -64.0f;
 // rounding in mg mu 2^f (mg mu is exact), ex2's error, and ldexp's exact
 // scaling (or its one rounding into the subnormal range).  Relative error
 // about 2^-21.  Below g = -200 the value is under 2^-152 for every finite
-// BF16 u, so it is a signed zero.  Not inlined: it runs only for such gates.
-__device__ __noinline__ float swiglu_far_negative(float g, float u) {
+// BF16 u, so it is a signed zero.
+__device__ __forceinline__ float swiglu_far_negative(float g, float u) {
   constexpr float kLog2eHi = 1.44268798828125f;   // 23637 / 16384
   constexpr float kLog2eLo = 7.0526077e-06f;      // log2(e) - kLog2eHi, rounded to float32
   if (g < -200.0f) return -copysignf(0.0f, u);    // the sign of g * u (g < 0)
@@ -887,22 +896,45 @@ __device__ __noinline__ float swiglu_far_negative(float g, float u) {
 
 // Two outputs v = BF16(silu(g) * u), silu(g) = g / (1 + e^-g) with
 // e^-g = 2^(-g log2 e); the multiplies and the add run as packed FP32x2
-// operations.  Relative error below 2^-16 for every gate: the rounding of
-// -g log2 e dominates (|g| log2(e) 2^-24 in the exponent, g >= -64 here) and
-// gates below -64 take swiglu_far_negative.  Flushing subnormals in ex2 and
-// rcp changes nothing that matters: a subnormal e^-g only adds to 1, a
-// subnormal g gives 2^0 = 1, and 1/inf = 0 as before.
+// operations.  Relative error below 2^-16 for g >= -64: the rounding of
+// -g log2 e dominates (|g| log2(e) 2^-24 in the exponent).  Flushing
+// subnormals in ex2 and rcp changes nothing that matters: a subnormal e^-g
+// only adds to 1, a subnormal g gives 2^0 = 1.
 __device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw) {
   constexpr float kLog2e = 1.4426950408889634f;
   const float2 g = make_float2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
   const float2 u = make_float2(__uint_as_float(uw << 16), __uint_as_float(uw & 0xFFFF0000u));
   const float2 t = __fmul2_rn(g, make_float2(-kLog2e, -kLog2e));
   const float2 d = __fadd2_rn(make_float2(ex2_ftz(t.x), ex2_ftz(t.y)), make_float2(1.0f, 1.0f));
-  float2 v = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
-  if (g.x < kFarNegativeGate) v.x = swiglu_far_negative(g.x, u.x);
-  if (g.y < kFarNegativeGate) v.y = swiglu_far_negative(g.y, u.y);
+  const float2 v = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
   const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);  // v.x in the low half
   return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Eight outputs (BF16 words of v) for the 8 gates in g and up values in up;
+// gates below -64 (rare: one integer test per 8 values) are redone with
+// swiglu_far_negative.
+__device__ __forceinline__ uint4 swiglu8(const uint4& g, const uint4& up) {
+  uint4 v;
+  v.x = swiglu_pair(g.x, up.x);
+  v.y = swiglu_pair(g.y, up.y);
+  v.z = swiglu_pair(g.z, up.z);
+  v.w = swiglu_pair(g.w, up.w);
+  if (any_far_negative(g)) {
+    uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {up.x, up.y, up.z, up.w}, vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t sh = (i & 1) * 16;
+      const uint32_t gb = (gw[i >> 1] >> sh) & 0xFFFFu;
+      if (gb > kFarNegativeBits) {
+        const float r = swiglu_far_negative(__uint_as_float(gb << 16), __uint_as_float(((uw[i >> 1] >> sh) & 0xFFFFu) << 16));
+        const uint32_t rb = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(r)));
+        vw[i >> 1] = (vw[i >> 1] & ~(0xFFFFu << sh)) | (rb << sh);
+      }
+    }
+    v = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+  }
+  return v;
 }
 
 __global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluParams p) {
@@ -923,11 +955,7 @@ __global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluPa
   const uint32_t hmask = 0xFFFFu << (t & 16);
   const int64_t rstep = static_cast<int64_t>(gridDim.x) * R;
   auto process = [&](int64_t row, int u, const uint4& g, const uint4& up) {
-    uint4 v;
-    v.x = swiglu_pair(g.x, up.x);
-    v.y = swiglu_pair(g.y, up.y);
-    v.z = swiglu_pair(g.z, up.z);
-    v.w = swiglu_pair(g.w, up.w);
+    const uint4 v = swiglu8(g, up);
     uint32_t m = umax_halves(absmax8_bits(v)) & 0xFFFFu;
 #pragma unroll
     for (int o = 1; o <= 8; o <<= 1) m = max(m, __shfl_xor_sync(hmask, m, o));  // the 16 lanes of a group

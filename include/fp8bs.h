@@ -234,6 +234,45 @@ int fp8bs_grouped_gemm(const uint8_t* a, const float* sa, int64_t M_total,
                        void* d, int d_dtype, int64_t N, int64_t K, void* stream);
 
 /*
+ * The block-scaled FP8 GEMM for power-of-two scales, with the scales applied
+ * by the tensor core: §3.5.2 (compute hardware) asks for tensor cores that
+ * take the group scaling factors themselves, so that partial sums need not
+ * be promoted to the CUDA cores for dequantisation; §3.3.2 notes the
+ * microscaling formats of the Blackwell generation.  Here the MMA is
+ * tcgen05.mma.kind::mxf8f6f4.block_scale: each group scale becomes an UE8M0
+ * scale (an 8-bit biased exponent) repeated over the group's four
+ * 32-element blocks of K, and all of K accumulates in FP32 in tensor memory.
+ *
+ *   D[m][n] (+)= sum_kb P_kb[m][n] * sa[kb*M + m] * s_b(n, kb)
+ *
+ * Same arguments, layouts, rules and errors as fp8bs_gemm, and the same
+ * result up to FP32 summation order, for operands whose scales are all
+ * powers of two: quantised with FP8BS_SCALE_POW2 (fp8bs_quantize_act_ex,
+ * fp8bs_quantize_weight_ex, fp8bs_requant_1x128_to_128x1).  Every scale of
+ * a row or column inside the output must be 0 (a group of zero codes) or a
+ * power of two in [2^-127, 2^127]; any other value is detected on the device
+ * and records FP8BS_ERR_DEVICE_ARG for fp8bs_get_device_status(), and D is
+ * then undefined.  The quantisers produce scales below 2^-127 only for
+ * groups whose absmax is below 448 * 2^-127; such operands need fp8bs_gemm.
+ */
+int fp8bs_gemm_pow2(const uint8_t* a, const float* sa,
+                    const uint8_t* b, const float* sb, int sb_kind,
+                    void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                    int accumulate, void* stream);
+
+/*
+ * Grouped (MoE) form of fp8bs_gemm_pow2: arguments, layouts, rules and
+ * errors of fp8bs_grouped_gemm, scales as fp8bs_gemm_pow2.  The activations
+ * dispatched to the experts carry power-of-two scales (§3.3.3
+ * "low-precision communication"); the expert weights must be quantised with
+ * FP8BS_SCALE_POW2 as well.
+ */
+int fp8bs_grouped_gemm_pow2(const uint8_t* a, const float* sa, int64_t M_total,
+                            const int32_t* offsets, int num_groups,
+                            const uint8_t* b, const float* sb,
+                            void* d, int d_dtype, int64_t N, int64_t K, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status of the
  * current device: FP8BS_OK, FP8BS_ERR_TIMEOUT, FP8BS_ERR_DEVICE_ARG, or
  * FP8BS_ERR_CUDA if the synchronisation itself failed.

@@ -95,8 +95,9 @@ def test_swiglu_quantize_argument_errors(lib):
     assert sq(None, 0, 128, 256, None, None, 0, None) == 0                        # empty: no-op
 
 
-def test_gemm_argument_errors(lib):
-    g = lib.fp8bs_gemm
+@pytest.mark.parametrize("name", ["fp8bs_gemm", "fp8bs_gemm_pow2"])
+def test_gemm_argument_errors(lib, name):
+    g = getattr(lib, name)
     assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 128, 100, 0, None) == 2   # K % 128
     assert g(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 100, 128, 0, None) == 2   # N % 128
     assert g(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 0, 128, 128, 128, 0, None) == 1   # scale kind
@@ -108,8 +109,9 @@ def test_gemm_argument_errors(lib):
     assert g(None, None, None, None, 0, None, 0, 0, 128, 128, 0, None) == 0     # empty: no-op
 
 
-def test_grouped_gemm_argument_errors(lib):
-    g = lib.fp8bs_grouped_gemm
+@pytest.mark.parametrize("name", ["fp8bs_grouped_gemm", "fp8bs_grouped_gemm_pow2"])
+def test_grouped_gemm_argument_errors(lib, name):
+    g = getattr(lib, name)
     assert g(FAKE, FAKE, 256, FAKE, 0, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # no groups
     assert g(FAKE, FAKE, 256, FAKE, 513, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1
     assert g(FAKE, FAKE, 256, None, 2, FAKE, FAKE, FAKE, 0, 128, 128, None) == 1      # offsets missing
