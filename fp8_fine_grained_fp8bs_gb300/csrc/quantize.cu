@@ -857,19 +857,12 @@ __device__ __forceinline__ float rcp_ftz(float x) {
   return y;
 }
 
-// Gates below -64 take swiglu_far_negative: there 1 + e^-g exceeds 2^92 and,
-// from about -87.3 on, its one-instruction reciprocal would flush to zero
-// although silu(g) * u is still a normal number.  As BF16 bit patterns these
-// gates are exactly the patterns above 0xC280 (-64.0; NaNs are outside the
-// contract).
+// Gates below -64 are redone by swiglu_far_negative when the fast form
+// flushed: there 1 + e^-g exceeds 2^92 and, from about -87.3 on, its
+// one-instruction reciprocal flushes to zero although silu(g) * u is still a
+// normal number.  As BF16 bit patterns these gates are exactly the patterns
+// above 0xC280 (-64.0; NaNs are outside the contract).
 constexpr uint32_t kFarNegativeBits = 0xC280u;
-
-// Whether any of the 8 BF16 gates in g lies below -64: the largest of the
-// 16-bit patterns, three two-lane maxima and one of the halves.
-__device__ __forceinline__ bool any_far_negative(const uint4& g) {
-  const uint32_t m = umax16x2(umax16x2(g.x, g.y), umax16x2(g.z, g.w));
-  return max(m & 0xFFFFu, m >> 16) > kFarNegativeBits;
-}
 
 // silu(g) * u for g < -64, where silu(g) = g e^g / (1 + e^g) and e^g < 2^-92,
 // so silu(g) * u = g u e^g to well within 2^-24.  Evaluated without overflow
@@ -896,44 +889,52 @@ __device__ __forceinline__ float swiglu_far_negative(float g, float u) {
 
 // Two outputs v = BF16(silu(g) * u), silu(g) = g / (1 + e^-g) with
 // e^-g = 2^(-g log2 e); the multiplies and the add run as packed FP32x2
-// operations.  Relative error below 2^-16 for g >= -64: the rounding of
-// -g log2 e dominates (|g| log2(e) 2^-24 in the exponent).  Flushing
-// subnormals in ex2 and rcp changes nothing that matters: a subnormal e^-g
-// only adds to 1, a subnormal g gives 2^0 = 1.
-__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw) {
+// operations.  Relative error below 2^-16 wherever the reciprocal does not
+// flush (the rounding of -g log2 e dominates: |g| log2(e) 2^-24 in the
+// exponent); the smallest reciprocal is kept in *rmin, and a zero there
+// means a gate below about -87.3 whose output swiglu8 redoes.  Flushing
+// subnormals in ex2 and rcp changes nothing else: a subnormal e^-g only adds
+// to 1, a subnormal g gives 2^0 = 1.
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t gw, uint32_t uw, float& rmin) {
   constexpr float kLog2e = 1.4426950408889634f;
   const float2 g = make_float2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
   const float2 u = make_float2(__uint_as_float(uw << 16), __uint_as_float(uw & 0xFFFF0000u));
   const float2 t = __fmul2_rn(g, make_float2(-kLog2e, -kLog2e));
   const float2 d = __fadd2_rn(make_float2(ex2_ftz(t.x), ex2_ftz(t.y)), make_float2(1.0f, 1.0f));
-  const float2 v = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
+  const float2 r = make_float2(rcp_ftz(d.x), rcp_ftz(d.y));
+  rmin = fminf(rmin, fminf(r.x, r.y));
+  const float2 v = __fmul2_rn(__fmul2_rn(g, r), u);
   const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);  // v.x in the low half
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// Eight outputs (BF16 words of v) for the 8 gates in g and up values in up;
-// gates below -64 (rare: one integer test per 8 values) are redone with
-// swiglu_far_negative.
-__device__ __forceinline__ uint4 swiglu8(const uint4& g, const uint4& up) {
-  uint4 v;
-  v.x = swiglu_pair(g.x, up.x);
-  v.y = swiglu_pair(g.y, up.y);
-  v.z = swiglu_pair(g.z, up.z);
-  v.w = swiglu_pair(g.w, up.w);
-  if (any_far_negative(g)) {
-    uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {up.x, up.y, up.z, up.w}, vw[4] = {v.x, v.y, v.z, v.w};
+// The outputs of the gates below -64 among 8 (g, up) pairs, redone with
+// swiglu_far_negative; the others are kept from v.  Runs only for groups of
+// 8 in which a reciprocal flushed, so it is kept out of line.
+__device__ __noinline__ uint4 swiglu8_far_negative(const uint4 g, const uint4 up, uint4 v) {
+  uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {up.x, up.y, up.z, up.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll 1
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t sh = (i & 1) * 16;
-      const uint32_t gb = (gw[i >> 1] >> sh) & 0xFFFFu;
-      if (gb > kFarNegativeBits) {
-        const float r = swiglu_far_negative(__uint_as_float(gb << 16), __uint_as_float(((uw[i >> 1] >> sh) & 0xFFFFu) << 16));
-        const uint32_t rb = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(r)));
-        vw[i >> 1] = (vw[i >> 1] & ~(0xFFFFu << sh)) | (rb << sh);
-      }
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t sh = (i & 1) * 16;
+    const uint32_t gb = (gw[i >> 1] >> sh) & 0xFFFFu;
+    if (gb > kFarNegativeBits) {
+      const float r = swiglu_far_negative(__uint_as_float(gb << 16), __uint_as_float(((uw[i >> 1] >> sh) & 0xFFFFu) << 16));
+      const uint32_t rb = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(r)));
+      vw[i >> 1] = (vw[i >> 1] & ~(0xFFFFu << sh)) | (rb << sh);
     }
-    v = make_uint4(vw[0], vw[1], vw[2], vw[3]);
   }
+  return make_uint4(vw[0], vw[1], vw[2], vw[3]);
+}
+
+// Eight outputs (BF16 words of v) for the 8 gates in g and up values in up.
+__device__ __forceinline__ uint4 swiglu8(const uint4& g, const uint4& up) {
+  float rmin = 1.0f;
+  uint4 v;
+  v.x = swiglu_pair(g.x, up.x, rmin);
+  v.y = swiglu_pair(g.y, up.y, rmin);
+  v.z = swiglu_pair(g.z, up.z, rmin);
+  v.w = swiglu_pair(g.w, up.w, rmin);
+  if (rmin == 0.0f) v = swiglu8_far_negative(g, up, v);
   return v;
 }
 
