@@ -74,9 +74,13 @@ def _peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _traffic(kernel_key: str, source_file: str):
+CSRC = "fp8_fine_grained_fp8bs_gb300/csrc/"
+
+
+def _traffic(kernel_key: str, *source_files: str):
     """DRAM bytes (read + write) per launch from the committed ncu summary, if
-    the kernel source still matches the one the counters were taken on."""
+    the kernel's sources (its .cu and the device headers it includes) still
+    match the ones the counters were taken on."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -85,8 +89,11 @@ def _traffic(kernel_key: str, source_file: str):
     e = d.get(kernel_key)
     if not e:
         return None
-    with open(os.path.join(ROOT, source_file), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    sha = hashlib.sha256()
+    for name in source_files:
+        with open(os.path.join(ROOT, name), "rb") as f:
+            sha.update(f.read())
+    h = sha.hexdigest()[:16]
     return e["dram_bytes_per_launch"] if e.get("source_sha256_16") == h else None
 
 
@@ -453,7 +460,64 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                                                        stream), stream, warmup, reps)
         out["moe_down"] = gemm_line(2.0 * real_rows * H * I, ms, rows=rows, real_rows=real_rows,
                                     shape=f"grouped {E} experts, [{rows} x {H} x {I}], BF16 out")
-        del aq, sa, bq, sb, y2, d_in, w_dn
+        del aq, sa, bq, sb, d_in, w_dn
+        # ---- the data movement around the expert GEMMs on one rank (the
+        # exchanges between ranks are the identity here): FP8 dispatch (pack
+        # the tokens' codes with row-major scales in send order, unpack into
+        # the experts' padded segments with kb-major scales) and BF16 combine
+        # (the expert outputs back in send order, then the gate-weighted sum)
+        from fp8_fine_grained_fp8bs_gb300 import moe as moe_plan
+        plan = moe_plan.MoePlan(choice, E, 1)
+        recv = moe_plan.exchange_counts(plan)
+        R, T_, nkb = plan.T * plan.k, plan.T, H // 128
+        xq_tok, sx_tok = fp8bs.quantize_act(x_tok, pow2=True)
+        send_idx = torch.from_numpy(plan.send_token).to(dev)
+        unpack_idx = torch.from_numpy(recv.unpack_idx).to(dev)
+        back_idx = torch.from_numpy(recv.back_idx).to(dev)
+        send_pos = torch.from_numpy(plan.send_pos).to(dev)
+        gate_w = torch.from_numpy(synth.moe_gate_weights(seed=rank, tokens=T_, top_k=plan.k)).to(dev)
+        q_send = torch.empty((R, H), dtype=torch.uint8, device=dev)
+        s_send = torch.empty((R, nkb), dtype=torch.float32, device=dev)
+        q_exp = torch.empty((recv.padded_rows, H), dtype=torch.uint8, device=dev)
+        s_exp = torch.empty((nkb, recv.padded_rows), dtype=torch.float32, device=dev)
+        row_b = H + 4 * nkb
+        ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, send_idx, R, q_send,
+                                                        s_send, fp8bs.SCALES_ROW_MAJOR, stream), stream, warmup, reps)
+        # each token's row is read from DRAM once (its k copies hit L2), each sent row written once
+        out["moe_dispatch_pack"] = bw_line(T_ * row_b + R * row_b + 4 * R, ms,
+                                           shape=f"{R} (token, expert) rows of E4M3 [{H}] + {nkb} scales gathered "
+                                                 f"from {T_} tokens in send order")
+        ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(q_send, s_send, R, H, fp8bs.SCALES_ROW_MAJOR, unpack_idx,
+                                                        recv.padded_rows, q_exp, s_exp, fp8bs.SCALES_KB_MAJOR, stream),
+                      stream, warmup, reps)
+        out["moe_dispatch_unpack"] = bw_line(R * row_b + recv.padded_rows * (row_b + 4), ms,
+                                             shape=f"{R} received rows into {E} expert segments padded to 128 "
+                                                   f"({recv.padded_rows} rows)")
+        direct_idx = torch.from_numpy(np.where(recv.unpack_idx >= 0,
+                                               plan.send_token[np.maximum(recv.unpack_idx, 0)], -1)
+                                      .astype(np.int32)).to(dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, direct_idx,
+                                                        recv.padded_rows, q_exp, s_exp, fp8bs.SCALES_KB_MAJOR, stream),
+                      stream, warmup, reps)
+        out["moe_dispatch_local"] = bw_line(T_ * row_b + recv.padded_rows * (row_b + 4), ms,
+                                            shape=f"one rank: {T_} tokens straight into {E} expert segments padded "
+                                                  f"to 128 ({recv.padded_rows} rows)")
+        y_back = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+        comb = torch.empty((T_, H), dtype=torch.bfloat16, device=dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_gather_bf16_rows(y2, rows, H, back_idx, R, y_back, stream), stream, warmup,
+                      reps)
+        out["moe_combine_gather"] = bw_line(2 * R * H * 2 + 4 * R, ms,
+                                            shape=f"{R} BF16 expert output rows [{H}] back in send order")
+        ms = _time_ms(lambda: fp8bs.fp8bs_moe_combine(y_back, R, H, send_pos, gate_w, T_, plan.k, comb, stream), stream,
+                      warmup, reps)
+        out["moe_combine"] = bw_line(R * H * 2 + T_ * H * 2 + 8 * R, ms,
+                                     shape=f"{T_} tokens x top-{plan.k}: gate-weighted BF16 sum in FP32 -> BF16 [{H}]")
+        local_pos = torch.from_numpy(recv.back_idx[plan.send_pos].astype(np.int32)).to(dev)
+        ms = _time_ms(lambda: fp8bs.fp8bs_moe_combine(y2, rows, H, local_pos, gate_w, T_, plan.k, comb, stream),
+                      stream, warmup, reps)
+        out["moe_combine_local"] = bw_line(R * H * 2 + T_ * H * 2 + 8 * R, ms,
+                                           shape="one rank: the same sum reading the expert rows in place")
+        del y2, xq_tok, sx_tok, q_send, s_send, q_exp, s_exp, y_back, comb, direct_idx, local_pos
     if "pow2" in sections:
         # ---- power-of-two scales applied by the tensor core (UE8M0 block
         # scales of tcgen05.mma.kind::mxf8f6f4), next to the fold GEMM on the
@@ -768,7 +832,7 @@ def main():
     line["roofline"] = {
         "bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
         "frac": gemm_tflops / fp8_peak,
-        "traffic": _traffic("gemm_dense_fprop_bf16", "fp8_fine_grained_fp8bs_gb300/csrc/gemm.cu"),
+        "traffic": _traffic("gemm_dense_fprop_bf16", *(CSRC + f for f in ("gemm.cu", "gemm_common.cuh", "common.cuh"))),
         "peak_source": f"{peak_src}: bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)",
         "hw_rate_peak": hw_peak, "frac_of_hw_rate": gemm_tflops / hw_peak,
         "hw_rate_source": f"{sms} SMs x 16384 FP8 FLOP/clk/SM x {max_mhz:g} MHz (maximum SM clock)"}
@@ -777,7 +841,7 @@ def main():
     line["quantize_roofline"] = {
         "bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
         "frac": q_gbs / peaks["hbm_gbs"],
-        "traffic": _traffic("quantize_act_1x128_16384x7168", "fp8_fine_grained_fp8bs_gb300/csrc/quantize.cu"),
+        "traffic": _traffic("quantize_act_1x128_16384x7168", *(CSRC + f for f in ("quantize.cu", "common.cuh"))),
         "peak_source": peak_src, "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS,
         "nominal_hbm_gbs": NOMINAL_HBM_GBS}
     line["quantize"] = {"gbs": q_gbs, "ms": q_ms, "frac_of_hbm": q_gbs / peaks["hbm_gbs"],

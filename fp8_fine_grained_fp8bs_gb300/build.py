@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfp8bs.so")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_mx.cu", "diag.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_mx.cu", "moe.cu", "diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr"]

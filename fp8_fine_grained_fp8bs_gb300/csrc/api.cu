@@ -266,6 +266,59 @@ int fp8bs_grouped_gemm_pow2(const uint8_t* a, const float* sa, int64_t M_total, 
   return run_gemm(g, true, stream);
 }
 
+int fp8bs_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, int s_in_layout,
+                        const int32_t* idx, int64_t rows_out, uint8_t* q_out, float* s_out, int s_out_layout,
+                        void* stream) {
+  if (rows_in < 0 || rows_out < 0 || H < 0) return FP8BS_ERR_INVALID_ARG;
+  if ((s_in_layout != FP8BS_SCALES_KB_MAJOR && s_in_layout != FP8BS_SCALES_ROW_MAJOR) ||
+      (s_out_layout != FP8BS_SCALES_KB_MAJOR && s_out_layout != FP8BS_SCALES_ROW_MAJOR))
+    return FP8BS_ERR_INVALID_ARG;
+  if (H % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (rows_in > (int64_t(1) << 31) - 1 || rows_out > (int64_t(1) << 31) || H > (int64_t(1) << 24))
+    return FP8BS_ERR_SHAPE;
+  if (rows_out == 0 || H == 0) return FP8BS_OK;
+  if (idx == nullptr || q_out == nullptr || s_out == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (rows_in > 0 && (q == nullptr || s == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(q_out)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_gather_q_rows(q, s, rows_in, H, s_in_layout == FP8BS_SCALES_KB_MAJOR, idx, rows_out,
+                                               q_out, s_out, s_out_layout == FP8BS_SCALES_KB_MAJOR, sms,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_gather_bf16_rows(const void* y, int64_t rows_in, int64_t N, const int32_t* idx, int64_t rows_out,
+                           void* out, void* stream) {
+  if (rows_in < 0 || rows_out < 0 || N < 0) return FP8BS_ERR_INVALID_ARG;
+  if (N % 8 != 0) return FP8BS_ERR_SHAPE;
+  if (rows_in > (int64_t(1) << 31) - 1 || rows_out > (int64_t(1) << 31) || N > (int64_t(1) << 24))
+    return FP8BS_ERR_SHAPE;
+  if (rows_out == 0 || N == 0) return FP8BS_OK;
+  if (idx == nullptr || out == nullptr || (rows_in > 0 && y == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_gather_bf16_rows(static_cast<const uint16_t*>(y), rows_in, N, idx, rows_out,
+                                                  static_cast<uint16_t*>(out), sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_moe_combine(const void* y, int64_t rows_y, int64_t N, const int32_t* idx, const float* w, int64_t T, int k,
+                      void* out, void* stream) {
+  if (rows_y < 0 || N < 0 || T < 0 || k < 1 || k > 64) return FP8BS_ERR_INVALID_ARG;
+  if (N % 8 != 0) return FP8BS_ERR_SHAPE;
+  if (rows_y > (int64_t(1) << 31) - 1 || T > (int64_t(1) << 31) / 64 || N > (int64_t(1) << 24)) return FP8BS_ERR_SHAPE;
+  if (T == 0 || N == 0) return FP8BS_OK;
+  if (idx == nullptr || w == nullptr || out == nullptr || (rows_y > 0 && y == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_moe_combine(static_cast<const uint16_t*>(y), rows_y, N, idx, w, T, k,
+                                             static_cast<uint16_t*>(out), sms, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_selftest_wait_timeout(int64_t timeout_us, void* stream) {
   if (timeout_us < 1 || timeout_us > 10000000) return FP8BS_ERR_INVALID_ARG;
   int sms = 0;

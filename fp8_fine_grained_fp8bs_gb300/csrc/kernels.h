@@ -74,6 +74,15 @@ cudaError_t launch_gemm_pow2(const GemmArgs& args, int sm_count, cudaStream_t st
                              bool* reg_check_failed);
 cudaError_t gemm_mx_take_status(int* status);
 
+// ---- moe.cu (row movement of the MoE dispatch and combine; no waits)
+cudaError_t launch_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, bool s_in_kb_major,
+                                 const int32_t* idx, int64_t rows_out, uint8_t* q_out, float* s_out,
+                                 bool s_out_kb_major, int sm_count, cudaStream_t stream);
+cudaError_t launch_gather_bf16_rows(const uint16_t* y, int64_t rows_in, int64_t N, const int32_t* idx,
+                                    int64_t rows_out, uint16_t* out, int sm_count, cudaStream_t stream);
+cudaError_t launch_moe_combine(const uint16_t* y, int64_t rows_y, int64_t N, const int32_t* idx, const float* w,
+                               int64_t T, int k, uint16_t* out, int sm_count, cudaStream_t stream);
+
 // Diagnostic: a kernel whose bounded wait runs out (nothing ever arrives on
 // its barrier) and records FP8BS_ERR_TIMEOUT in the GEMM status word.
 cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, cudaStream_t stream);

@@ -37,6 +37,7 @@ TID_W_GATE_UP = 5
 TID_W_DOWN = 6
 TID_ROUTING = 7
 TID_DOWN_IN = 8
+TID_GATE = 9
 TID_OUTLIER = 1000  # added to the tensor id of the tensor that gets outliers
 
 _CHUNK = 1 << 22
@@ -118,6 +119,14 @@ def moe_routing(seed: int = 0, tokens: int = 8192, experts: int = 32, top_k: int
     gumbel = -np.log(-np.log(g.random((tokens, experts))))
     keys = logw[None, :] + gumbel
     return np.argsort(-keys, axis=1, kind="stable")[:, :top_k].astype(np.int32)
+
+
+def moe_gate_weights(seed: int = 0, tokens: int = 8192, top_k: int = 8) -> np.ndarray:
+    """Gate weights [tokens, top_k] float32 of the routed experts: positive,
+    each token's weights normalised to sum to 1 (uniform draws in (0.05, 1))."""
+    g = _rng(seed, TID_GATE)
+    w = g.uniform(0.05, 1.0, (tokens, top_k)).astype(np.float32)
+    return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
 def moe_layout(choice: np.ndarray, experts: int = 32, align: int = 128):

@@ -272,6 +272,62 @@ int fp8bs_grouped_gemm_pow2(const uint8_t* a, const float* sa, int64_t M_total,
                             const uint8_t* b, const float* sb,
                             void* d, int d_dtype, int64_t N, int64_t K, void* stream);
 
+/* Layout of the float32 scales of a matrix of E4M3 codes [rows][H] (1x128
+ * groups) in fp8bs_gather_q_rows. */
+typedef enum {
+  FP8BS_SCALES_KB_MAJOR = 0,  /* s[kb * rows + r]: the layout every GEMM reads */
+  FP8BS_SCALES_ROW_MAJOR = 1  /* s[r * (H/128) + kb]: one contiguous record per row */
+} fp8bs_scale_layout;
+
+/*
+ * Row gather of FP8 codes with their 1x128 scales, the data movement of the
+ * MoE dispatch (§3.3.3 "low-precision communication": the activations are
+ * quantised to FP8, with power-of-two scales, before they are dispatched to
+ * the experts, so the FP8 bytes and scales are what moves; the expert GEMMs
+ * consume them directly):
+ *
+ *   q_out[i][:] = q[idx[i]][:],  scales of out row i = scales of row idx[i];
+ *   idx[i] < 0 (or >= rows_in): a row of zero codes with zero scales (the
+ *   padding of an expert's segment to a multiple of 128 rows).
+ *
+ *   q      [rows_in][H] E4M3 codes.  s: float32 scales in s_in_layout.   (in)
+ *   idx    DEVICE int32 [rows_out].                                       (in)
+ *   q_out  [rows_out][H] E4M3.  s_out: float32 scales in s_out_layout.   (out)
+ * Packing the rows a rank sends into one buffer per destination (row-major
+ * scales: one record per row travels with it) and unpacking received rows
+ * into the experts' padded segments (kb-major scales, as the grouped GEMM
+ * reads them) are both this call.
+ * Rules: H % 128 == 0; q, q_out 16-byte aligned; the layouts are
+ * fp8bs_scale_layout values (FP8BS_ERR_INVALID_ARG otherwise).
+ */
+int fp8bs_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, int s_in_layout,
+                        const int32_t* idx, int64_t rows_out, uint8_t* q_out, float* s_out, int s_out_layout,
+                        void* stream);
+
+/*
+ * Row gather of a BF16 matrix (the expert outputs put back in send order for
+ * the combine, which §3.3.3 keeps in BF16):
+ *   out[i][:] = y[idx[i]][:], zeros where idx[i] < 0 or >= rows_in.
+ *   y [rows_in][N] BF16; idx DEVICE int32 [rows_out]; out [rows_out][N] BF16.
+ * Rules: N % 8 == 0; y, out 16-byte aligned.
+ */
+int fp8bs_gather_bf16_rows(const void* y, int64_t rows_in, int64_t N, const int32_t* idx, int64_t rows_out,
+                           void* out, void* stream);
+
+/*
+ * The MoE combine in BF16 (§3.3.3: the combine components stay in BF16):
+ *   out[t][n] = BF16_rne( sum_{j<k} w[t][j] * y[idx[t][j]][n] ),
+ * the products and the sum in FP32 (fused multiply-adds, j ascending) and one
+ * rounding to BF16; idx[t][j] < 0 (or >= rows_y) contributes nothing.
+ *   y    [rows_y][N] BF16: the expert outputs, one row per (token, expert).
+ *   idx  DEVICE int32 [T][k]: the row of y holding token t's j-th expert output.
+ *   w    DEVICE float32 [T][k]: the gate weights.
+ *   out  [T][N] BF16.
+ * Rules: N % 8 == 0; 1 <= k <= 64; y, out 16-byte aligned.
+ */
+int fp8bs_moe_combine(const void* y, int64_t rows_y, int64_t N, const int32_t* idx, const float* w, int64_t T, int k,
+                      void* out, void* stream);
+
 /*
  * Synchronises `stream`, then returns and clears the device status of the
  * current device: FP8BS_OK, FP8BS_ERR_TIMEOUT, FP8BS_ERR_DEVICE_ARG, or

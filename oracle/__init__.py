@@ -42,11 +42,12 @@ from .quantize import (quantize_groups, quantize_act_1x128, quantize_act_128x1,
                        dequantize_1x128, requant_1x128_to_128x1, swiglu, bf16_round_f64,
                        swiglu_quantize_1x128)
 from .gemm import gemm_block_scaled, grouped_gemm_block_scaled, bf16_round
+from .moe import moe_combine
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_all_finite_values",
     "quantize_groups", "quantize_act_1x128", "quantize_act_128x1",
     "quantize_weight_128x128", "bf16_bits_to_f32", "pow2_scale",
     "dequantize_1x128", "requant_1x128_to_128x1", "swiglu", "bf16_round_f64", "swiglu_quantize_1x128",
-    "gemm_block_scaled", "grouped_gemm_block_scaled", "bf16_round",
+    "gemm_block_scaled", "grouped_gemm_block_scaled", "bf16_round", "moe_combine",
 ]

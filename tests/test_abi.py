@@ -119,6 +119,21 @@ def test_grouped_gemm_argument_errors(lib, name):
     assert g(FAKE, FAKE, 256, FAKE, 2, FAKE, FAKE, FAKE + 1, 0, 128, 128, None) == 3
 
 
+def test_moe_row_kernels_argument_errors(lib):
+    gq, gb, cb = lib.fp8bs_gather_q_rows, lib.fp8bs_gather_bf16_rows, lib.fp8bs_moe_combine
+    assert gq(FAKE, FAKE, 10, 100, 0, FAKE, 10, FAKE, FAKE, 1, None) == 2      # H % 128
+    assert gq(FAKE, FAKE, 10, 128, 2, FAKE, 10, FAKE, FAKE, 1, None) == 1      # unknown scale layout
+    assert gq(FAKE, FAKE, 10, 128, 0, None, 10, FAKE, FAKE, 1, None) == 1      # no index
+    assert gq(FAKE + 4, FAKE, 10, 128, 0, FAKE, 10, FAKE, FAKE, 1, None) == 3
+    assert gq(None, None, 0, 128, 0, None, 0, None, None, 0, None) == 0        # empty: no-op
+    assert gb(FAKE, 10, 12, FAKE, 10, FAKE, None) == 2                         # N % 8
+    assert gb(FAKE, 10, 16, FAKE, 10, FAKE + 2, None) == 3
+    assert cb(FAKE, 10, 16, FAKE, FAKE, 4, 0, FAKE, None) == 1                 # k < 1
+    assert cb(FAKE, 10, 16, FAKE, FAKE, 4, 65, FAKE, None) == 1                # k > 64
+    assert cb(FAKE, 10, 12, FAKE, FAKE, 4, 2, FAKE, None) == 2
+    assert cb(FAKE, 10, 16, None, FAKE, 4, 2, FAKE, None) == 1
+
+
 def test_quantize_act_weight_argument_errors(lib):
     q = lib.fp8bs_quantize_act_weight
     ok = (FAKE, 128, 256, 256, FAKE, FAKE, FAKE, 128, 256, 256, FAKE, FAKE, 0, None)
