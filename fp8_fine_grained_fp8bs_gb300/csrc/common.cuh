@@ -341,6 +341,16 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
 
 // 32 lanes x 32 consecutive 32-bit TMEM columns: thread i of the warp gets
 // lane (base lane + i), columns c .. c+31.
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may begin while the kernel before it on the stream is still
+// running; griddep_wait() returns once that kernel has completed and its
+// memory operations are visible (at once when there is no such kernel).  A
+// producer calls griddep_launch_dependents() to let the dependent grid be
+// scheduled as its CTAs leave the SMs (it is launched once every CTA of the
+// producer has called it or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "

@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&teardown[0], 1);
     mbar_init(&teardown[1], 1);
     fence_barrier_init();
+    griddep_wait();  // the group table below may come from the preceding kernel
     // tile count (and, for the grouped GEMM, the validated group table)
     int total_mt = 0;
     bool ok = true;
@@ -227,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   if (kPair) cluster_sync();  // the peer's barriers exist before anything signals them
+  // Launched behind another kernel (programmatic dependent launch), the
+  // set-up above overlaps that kernel's tail; operands, scales and D are
+  // touched only after it has completed.
+  griddep_wait();
   const uint32_t tmem_base = misc[0];
   const int total_tiles = static_cast<int>(misc[2]);
   volatile uint32_t* abort_flag = &misc[1];
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int row0, n0;
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
-        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
+        for (int kb = 0; kb < p.nkb; ++kb) {
           if (!warp_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
           if (lane == 0) {
             if (kPair) {
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         const bool last_tile = t + nunits >= total_tiles;
-        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, ++step, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
+        for (int kb = 0; kb < p.nkb; ++kb, ++step) {
           const uint32_t chunk = (step / C::kScaleChunk) % kScaleChunks;
           if (step % C::kScaleChunk == 0 &&
               !mbar_wait(&sc_empty[chunk], ((step / C::kScaleSlots) & 1u) ^ 1u, p.timeout_ns)) {
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nb = static_cast<int64_t>(g) * nnb + n0 / 128 + lane;
             cp_async_4(dst + kBlockM + lane, p.sb + nb * p.nkb + kb);
           }
-          if (step % C::kScaleChunk == C::kScaleChunk - 1 || (last_tile && kk + 1 == p.nkb))
+          if (step % C::kScaleChunk == C::kScaleChunk - 1 || (last_tile && kb + 1 == p.nkb))
             cp_async_mbar_arrive(&sc_full[chunk]);
         }
       }
@@ -430,16 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* scol = scs + kBlockM + colhalf * C::kColsPerThread;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                colhalf * C::kColsPerThread;
-        // TMEM -> registers 64 columns per round; the buffer is handed back
-        // to the MMA as soon as the last round has landed.
+        // TMEM -> registers 32 columns at a time, the next chunk's load in
+        // flight while the current one is folded; the buffer is handed back
+        // to the MMA as soon as the last chunk has landed.
+        uint32_t rr[2][32];
+        tmem_ld32(taddr, rr[0]);
+        tmem_wait_ld(rr[0]);
 #pragma unroll
-        for (int ch = 0; ch < C::kChunks; ch += 2) {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(taddr + ch * 32, ra);
-          tmem_ld32(taddr + (ch + 1) * 32, rb);
-          tmem_wait_ld(ra);
-          tmem_wait_ld(rb);
-          if (ch + 2 == C::kChunks) {
+        for (int ch = 0; ch < C::kChunks; ++ch) {
+          if (ch + 1 < C::kChunks) {
+            tmem_ld32(taddr + (ch + 1) * 32, rr[(ch + 1) & 1]);
+          } else {
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -449,13 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&t_empty[buf]);
             }
           }
-          if (kRowScale) {
-            fold_row(acc2 + ch * 16, ra, s_ab, scol + ch * 32);
-            fold_row(acc2 + (ch + 1) * 16, rb, s_ab, scol + (ch + 1) * 32);
-          } else {
-            fold_block(acc2 + ch * 16, ra, s_ab);
-            fold_block(acc2 + (ch + 1) * 16, rb, s_ab);
-          }
+          if (kRowScale)
+            fold_row(acc2 + ch * 16, rr[ch & 1], s_ab, scol + ch * 32);
+          else
+            fold_block(acc2 + ch * 16, rr[ch & 1], s_ab);
+          if (ch + 1 < C::kChunks) tmem_wait_ld(rr[(ch + 1) & 1]);
         }
         if (step % C::kScaleChunk == C::kScaleChunk - 1) {
           __syncwarp();
@@ -553,32 +557,9 @@ cudaError_t run(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* tmap
   if (kPair) mt_bound = (mt_bound + 1) / 2;
   const int64_t units = mt_bound * ntn;
   if (units <= 0) return cudaSuccess;
-  if (!kPair) {
-    const int grid = static_cast<int>(std::min<int64_t>(units, sm_count));
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmA, tmB, tmD, kp);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 2;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
   static std::atomic<int> cluster_cache[kMaxCachedDevices];  // co-resident clusters, per device
-  int max_clusters = 0;
-  cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
-  err = cached_per_device(cluster_cache, [&](int* n) { return cudaOccupancyMaxActiveClusters(n, kern, &cfg); },
-                          &max_clusters);
-  if (err != cudaSuccess) return err;
-  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, kp);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
+  return launch_persistent<kPair>(kern, units, sm_count, kThreads, C::kSmemBytes, stream, cluster_cache, tmA, tmB,
+                                  tmD, kp);
 }
 
 }  // namespace

@@ -7,6 +7,9 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "tmap.h"
 
@@ -113,11 +116,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 // segment: that CTA still loads its half of B and joins the MMA, and stores
 // nothing (row0 >= row_end).
 //
-// Every role walks the k-blocks of work unit t starting at t % (K/128) and
-// wrapping around: CTAs that share an A or B tile then read different
-// k-slices of it at any moment instead of all hitting the same lines.  The
-// blocks are summed in that order (the sum is the same up to FP32 rounding
-// order).
+// Every role walks the k-blocks of a unit in order, so the CTAs that share
+// an A or B tile read its k-slices at about the same time and the second
+// reader finds them in L2 (when A and B together exceed L2, as in Wgrad,
+// starting each unit at its own k-block cost 9% with the scales in the MMA).
 template <int BN, bool kPair>
 __device__ __forceinline__ void tile_coords(int t, int ntn, bool grouped, const int* s_off, const int* s_cum,
                                             int num_groups, uint32_t rank, int64_t M, int& row0, int& n0, int& g,
@@ -173,6 +175,47 @@ bool encode_output(CUtensorMap* map, void* base, int64_t rows, int64_t N, bool b
                          gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Launches a persistent GEMM grid: one CTA per SM, or with kPair one
+// cluster of two CTAs per SM pair (as many clusters as can be co-resident),
+// or fewer when there are fewer work units.  The launch allows programmatic
+// stream serialisation: the kernel's set-up (barriers, tensor memory, tensor
+// map prefetch) overlaps the tail of the kernel before it on the stream, and
+// the kernel calls griddep_wait() before it touches memory.
+template <bool kPair, typename Kern, typename... Args>
+cudaError_t launch_persistent(Kern kern, int64_t units, int sm_count, int threads, int smem_bytes,
+                              cudaStream_t stream, std::atomic<int> (&cluster_cache)[kMaxCachedDevices],
+                              Args... args) {
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  if (!kPair) {
+    cfg.attrs = attrs + 1;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(units, sm_count)), 1, 1);
+  } else {
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count / 2)), 1, 1);
+    int max_clusters = 0;
+    const cudaError_t e = cached_per_device(
+        cluster_cache, [&](int* n) { return cudaOccupancyMaxActiveClusters(n, kern, &cfg); }, &max_clusters);
+    if (e != cudaSuccess) return e;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace

@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     mbar_init(&teardown[0], 1);
     fence_barrier_init();
+    griddep_wait();  // the group table below may come from the preceding kernel
     int total_mt = 0;
     bool ok = true;
     if (kGrouped) {
@@ -301,6 +302,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   if (kPair) cluster_sync();
+  // Launched behind another kernel (programmatic dependent launch), the
+  // set-up above overlaps that kernel's tail; operands, scales and D are
+  // touched only after it has completed.
+  griddep_wait();
   const uint32_t tmem_base = misc[0];
   const int total_tiles = static_cast<int>(misc[2]);
   volatile uint32_t* abort_flag = &misc[1];
@@ -319,18 +324,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         int row0, n0;
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
-        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
+        for (int kb = 0; kb < p.nkb; ++kb) {
           if (!warp_wait(&empty[stage], phase ^ 1, p.timeout_ns)) { live = false; break; }
           // The slot's scales are in shared memory (both CTAs') before its
           // first stage is loaded: a full stage then implies ready scales,
           // and the MMA thread waits on the stage alone.
-          if (rank == 0 && kk % kStepsPerSlot == 0) {
+          if (rank == 0 && kb % kStepsPerSlot == 0) {
             const bool ok = __shfl_sync(0xffffffffu,
                                         mbar_wait_cluster(&sf_full[gs % C::kSfSlots], (gs / C::kSfSlots) & 1u,
                                                           p.timeout_ns), 0);
             ++gs;
             if (!ok) { live = false; break; }
-          } else if (kk % kStepsPerSlot == 0) {
+          } else if (kb % kStepsPerSlot == 0) {
             ++gs;
           }
           if (lane == 0) {
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         int64_t row_end;
         tile_coords<BN, kPair>(t, ntn, kGrouped, s_off, s_cum, p.num_groups, rank, p.M, row0, n0, g, row_end);
         const bool last_tile = t + nunits >= total_tiles;
-        for (int kk = 0, kb = t % p.nkb; kk < p.nkb; ++kk, ++step, kb = (kb + 1 == p.nkb) ? 0 : kb + 1) {
+        for (int kb = 0; kb < p.nkb; ++kb, ++step) {
           const uint32_t chunk = (step / C::kScaleChunk) % kMxScaleChunks;
           if (step % C::kScaleChunk == 0 &&
               !mbar_wait(&sc_empty[chunk], ((step / C::kScaleSlots) & 1u) ^ 1u, p.timeout_ns)) {
@@ -484,7 +489,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const int64_t nb = static_cast<int64_t>(g) * nnb + n0 / 128 + lane;
             cp_async_4(dst + kBlockM + lane, p.sb + nb * p.nkb + kb);
           }
-          if (step % C::kScaleChunk == C::kScaleChunk - 1 || (last_tile && kk + 1 == p.nkb))
+          if (step % C::kScaleChunk == C::kScaleChunk - 1 || (last_tile && kb + 1 == p.nkb))
             cp_async_mbar_arrive(&sc_full[chunk]);
         }
       }
@@ -730,32 +735,9 @@ cudaError_t run_mx(const GemmArgs& a, int sm_count, cudaStream_t stream, bool* t
   if (kPair) mt_bound = (mt_bound + 1) / 2;
   const int64_t units = mt_bound * ntn;
   if (units <= 0) return cudaSuccess;
-  if (!kPair) {
-    const int grid = static_cast<int>(std::min<int64_t>(units, sm_count));
-    kern<<<grid, kMxThreads, C::kSmemBytes, stream>>>(tmA, tmB, tmD, kp);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 2;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kMxThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  static std::atomic<int> cluster_cache[kMaxCachedDevices];
-  int max_clusters = 0;
-  cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
-  err = cached_per_device(cluster_cache, [&](int* n) { return cudaOccupancyMaxActiveClusters(n, kern, &cfg); },
-                          &max_clusters);
-  if (err != cudaSuccess) return err;
-  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<int64_t>(units, max_clusters)), 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, kp);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
+  static std::atomic<int> cluster_cache[kMaxCachedDevices];  // co-resident clusters, per device
+  return launch_persistent<kPair>(kern, units, sm_count, kMxThreads, C::kSmemBytes, stream, cluster_cache, tmA, tmB,
+                                  tmD, kp);
 }
 
 }  // namespace

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kMoeThreads) gather_q_rows_kernel(const uint8_
                                                                      const int32_t* __restrict__ idx, int64_t rows_out,
                                                                      uint8_t* __restrict__ q_out,
                                                                      float* __restrict__ s_out, int s_out_kb_major) {
+  griddep_launch_dependents();  // the grouped GEMM on the gathered rows may start its set-up
   const int lane = threadIdx.x & 31;
   const int64_t nkb = H / kGroup;
   const int64_t vec = H / 16;  // 16-byte pieces of a row of codes

@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                       const TileParams p, const TileParams pw) {
   using Q = QCfg<kMode>;
+  griddep_launch_dependents();  // a GEMM launched behind this kernel may start its set-up
   extern __shared__ uint8_t qsmem_raw[];
   // 1024-byte aligned base, offset from the shared array itself so that the
   // compiler keeps the shared address space (shared loads and stores rather
@@ -730,6 +731,7 @@ __device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
 }
 
 __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantParams p) {
+  griddep_launch_dependents();
   __shared__ float colred[kRqThreads / 32][kGroup];     // per-warp column maxima of |v|
   __shared__ float2 coldiv[kGroup];                     // per column: (s, RN(1/s)), fast path flag in the sign of y
   // Output tile: row R of X^T's tile (tile column R) as 16 units of 8 codes;
@@ -939,6 +941,7 @@ __device__ __forceinline__ uint4 swiglu8(const uint4& g, const uint4& up) {
 }
 
 __global__ void __launch_bounds__(kSgThreads) swiglu_quant_kernel(const SwigluParams p) {
+  griddep_launch_dependents();
   __shared__ DivTable tab;
   div_table_init(tab);
   __syncthreads();
