@@ -122,13 +122,20 @@ __device__ __forceinline__ void fold_block(float2* acc, const uint32_t (&p)[32],
     acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), s2, acc[j]);
 }
 
-// acc[j] += p[j] * (s_a * s_b[j]) with per-column scales s_b (Wgrad).
-__device__ __forceinline__ void fold_row(float2* acc, const uint32_t (&p)[32], float sa, const float* sb) {
-  const float2 sa2 = make_float2(sa, sa);
+// Row-scaled B in the fragment layout of tcgen05.ld.16x256b: p holds, for
+// 8-column groups g = 0..3, columns 8g + 2(lane % 4) + {0, 1} of two rows
+// (registers 4g, 4g+1 of the first, 4g+2, 4g+3 of the second, 8 rows
+// further); acc[2g + j] += p * (s_a[j] * s_b of the column pair g).
+__device__ __forceinline__ void fold_frag(float2* acc, const uint32_t (&p)[16], float sa0, float sa1,
+                                          const float2* sb) {
+  const float2 a0 = make_float2(sa0, sa0);
+  const float2 a1 = make_float2(sa1, sa1);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float2 c = __fmul2_rn(sa2, *reinterpret_cast<const float2*>(sb + 2 * j));
-    acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), c, acc[j]);
+  for (int g = 0; g < 4; ++g) {
+    acc[2 * g] = __ffma2_rn(make_float2(__uint_as_float(p[4 * g]), __uint_as_float(p[4 * g + 1])),
+                            __fmul2_rn(a0, sb[g]), acc[2 * g]);
+    acc[2 * g + 1] = __ffma2_rn(make_float2(__uint_as_float(p[4 * g + 2]), __uint_as_float(p[4 * g + 3])),
+                                __fmul2_rn(a1, sb[g]), acc[2 * g + 1]);
   }
 }
 
@@ -427,39 +434,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           live = false;
           break;
         }
-        if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
-        tc_fence_after_sync();
         const float* scs = sScale + (step % C::kScaleSlots) * C::kSlotFloats;
-        const float sa = scs[row_in_tile];
-        const float s_ab = kRowScale ? sa : sa * scs[kBlockM + bsel];
-        const float* scol = scs + kBlockM + colhalf * C::kColsPerThread;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
-                               colhalf * C::kColsPerThread;
-        // TMEM -> registers 32 columns at a time, the next chunk's load in
-        // flight while the current one is folded; the buffer is handed back
-        // to the MMA as soon as the last chunk has landed.
-        uint32_t rr[2][32];
-        tmem_ld32(taddr, rr[0]);
-        tmem_wait_ld(rr[0]);
+        if constexpr (kRowScale) {
+          // Per-column scales: the partial is read in the fragment layout of
+          // tcgen05.ld.16x256b, where a thread holds 8 of every 32 columns
+          // (of 4 rows), so it needs a quarter of the column scales a
+          // row-per-thread layout needs: per 32-column chunk 4 pairs, loaded
+          // one chunk ahead (the first chunk's and the 4 row scales before
+          // the wait for the partial).
+          float sa4[4];
 #pragma unroll
-        for (int ch = 0; ch < C::kChunks; ++ch) {
-          if (ch + 1 < C::kChunks) {
-            tmem_ld32(taddr + (ch + 1) * 32, rr[(ch + 1) & 1]);
-          } else {
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-              if (kPair)
-                mbar_arrive_cluster(mapa_shared(&t_empty[buf], 0));  // the leader's MMA waits on it
-              else
-                mbar_arrive(&t_empty[buf]);
+          for (int i = 0; i < 4; ++i) sa4[i] = scs[quarter * 32 + 8 * i + (lane >> 2)];
+          const float* scol = scs + kBlockM + colhalf * C::kColsPerThread + 2 * (lane & 3);
+          float2 sbc[2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sbc[0][i] = *reinterpret_cast<const float2*>(scol + 8 * i);
+          if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
+          tc_fence_after_sync();
+          const uint32_t tcol = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
+                                colhalf * C::kColsPerThread;
+          // pieces (32-column chunk c, 16-lane half h), chunk-major, the next
+          // piece's load in flight while the current one is folded
+          constexpr int kFrag = 2 * C::kChunks;
+          uint32_t fr[2][16];
+          tmem_ld16x256b_x4(tcol, fr[0]);
+          tmem_wait_ld(fr[0]);
+#pragma unroll
+          for (int f = 0; f < kFrag; ++f) {
+            const int h = f & 1, c = f >> 1;
+            if (h == 0 && c + 1 < C::kChunks) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                sbc[(c + 1) & 1][i] = *reinterpret_cast<const float2*>(scol + 32 * (c + 1) + 8 * i);
             }
+            if (f + 1 < kFrag) {
+              const int nh = (f + 1) & 1, nc = (f + 1) >> 1;
+              tmem_ld16x256b_x4(tcol + (static_cast<uint32_t>(16 * nh) << 16) + 32 * nc, fr[(f + 1) & 1]);
+            } else {
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) {
+                if (kPair)
+                  mbar_arrive_cluster(mapa_shared(&t_empty[buf], 0));  // the leader's MMA waits on it
+                else
+                  mbar_arrive(&t_empty[buf]);
+              }
+            }
+            fold_frag(acc2 + (h * C::kChunks + c) * 8, fr[f & 1], sa4[2 * h], sa4[2 * h + 1], sbc[c & 1]);
+            if (f + 1 < kFrag) tmem_wait_ld(fr[(f + 1) & 1]);
           }
-          if (kRowScale)
-            fold_row(acc2 + ch * 16, rr[ch & 1], s_ab, scol + ch * 32);
-          else
+        } else {
+          if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
+          tc_fence_after_sync();
+          const float sa = scs[row_in_tile];
+          const float s_ab = sa * scs[kBlockM + bsel];
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
+                                 colhalf * C::kColsPerThread;
+          // TMEM -> registers 32 columns at a time, the next chunk's load in
+          // flight while the current one is folded; the buffer is handed back
+          // to the MMA as soon as the last chunk has landed.
+          uint32_t rr[2][32];
+          tmem_ld32(taddr, rr[0]);
+          tmem_wait_ld(rr[0]);
+#pragma unroll
+          for (int ch = 0; ch < C::kChunks; ++ch) {
+            if (ch + 1 < C::kChunks) {
+              tmem_ld32(taddr + (ch + 1) * 32, rr[(ch + 1) & 1]);
+            } else {
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) {
+                if (kPair)
+                  mbar_arrive_cluster(mapa_shared(&t_empty[buf], 0));  // the leader's MMA waits on it
+                else
+                  mbar_arrive(&t_empty[buf]);
+              }
+            }
             fold_block(acc2 + ch * 16, rr[ch & 1], s_ab);
-          if (ch + 1 < C::kChunks) tmem_wait_ld(rr[(ch + 1) & 1]);
+            if (ch + 1 < C::kChunks) tmem_wait_ld(rr[(ch + 1) & 1]);
+          }
         }
         if (step % C::kScaleChunk == C::kScaleChunk - 1) {
           __syncwarp();
@@ -473,10 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* acc = reinterpret_cast<const float*>(acc2);
       const int y0 = row0 + quarter * 32;
       if (y0 < row_end && ncol0 < p.N) {
-        if (p.out_bf16)
-          store_segment<C::kColsPerThread, true>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, false);
-        else
-          store_segment<C::kColsPerThread, false>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, p.accumulate != 0);
+        if constexpr (kRowScale) {
+          if (p.out_bf16)
+            store_segment_frag<C::kColsPerThread, true>(acc2, s_out, out_seq, lane, &tmD, ncol0, y0, false);
+          else
+            store_segment_frag<C::kColsPerThread, false>(acc2, s_out, out_seq, lane, &tmD, ncol0, y0,
+                                                         p.accumulate != 0);
+        } else {
+          if (p.out_bf16)
+            store_segment<C::kColsPerThread, true>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, false);
+          else
+            store_segment<C::kColsPerThread, false>(acc, s_out, out_seq, lane, &tmD, ncol0, y0, p.accumulate != 0);
+        }
       }
     }
     // the staging boxes stay in use until the last stores have completed

@@ -95,6 +95,58 @@ __device__ __forceinline__ void store_segment(const float* acc, uint8_t* slots, 
   }
 }
 
+// The same store for a warp whose accumulators are in the fragment layout
+// of tcgen05.ld.16x256b (the fold with per-column scales):
+// acc2[((h * (kCols / 32) + c) * 4 + g) * 2 + j] holds columns
+// x0 + 32c + 8g + 2(lane % 4) + {0, 1} of row y0 + 16h + 8j + lane / 4.
+// Same staging boxes, swizzle and TMA stores as store_segment.
+template <int kCols, bool kBf16, int kSlots = kOutSlots>
+__device__ __forceinline__ void store_segment_frag(const float2* acc2, uint8_t* slots, uint32_t& seq, int lane,
+                                                   const CUtensorMap* tmD, int x0, int y0, bool add) {
+  constexpr int kChunks = kCols / 32;
+  constexpr int kBoxCols = kBf16 ? 64 : 32;  // columns in 128 bytes
+  constexpr int kChunksPerBox = kBoxCols / 32;
+  static_assert(kCols % kBoxCols == 0, "segment of whole boxes");
+  const int q4 = lane & 3;
+#pragma unroll
+  for (int b = 0; b < kCols / kBoxCols; ++b, ++seq) {
+    uint8_t* box = slots + (seq % kSlots) * kOutBoxBytes;
+    if (lane == 0) bulk_wait_read<kSlots - 1>();
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int row = 16 * h + 8 * j + (lane >> 2);
+        uint8_t* rowp = box + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < kChunksPerBox; ++cc) {
+          const int c = b * kChunksPerBox + cc;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float2 v = acc2[((h * kChunks + c) * 4 + g) * 2 + j];
+            if (kBf16) {  // bytes 64cc + 16g + 4(lane % 4) of the row
+              *reinterpret_cast<uint32_t*>(rowp + (((4 * cc + g) ^ (row & 7)) << 4) + 4 * q4) =
+                  pack_bf16x2(v.x, v.y);
+            } else {      // bytes 32g + 8(lane % 4) of the row
+              *reinterpret_cast<float2*>(rowp + (((2 * g + (q4 >> 1)) ^ (row & 7)) << 4) + 8 * (q4 & 1)) = v;
+            }
+          }
+        }
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      if (add)
+        tma_reduce_add_2d(tmD, box, x0 + b * kBoxCols, y0);
+      else
+        tma_store_2d(tmD, box, x0 + b * kBoxCols, y0);
+      bulk_commit();
+    }
+  }
+}
+
 // A bounded mbarrier wait made by a whole warp, with lane 0's outcome.  The
 // producer and MMA-issuer warps run their loops converged (lane 0 issues
 // the copies and MMAs): a warp whose lane 0 loops alone while its other

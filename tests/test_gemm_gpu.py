@@ -192,6 +192,39 @@ def test_wgrad_full_size_sampled():
     check_f32(dw[np.ix_(rows, cols)], Y, Tm, "wgrad")
 
 
+@pytest.mark.parametrize("M, N, K", [(256, 384, 512), (200, 256, 384), (2300, 2176, 256)])
+@pytest.mark.parametrize("out", ["f32", "bf16", "f32_accumulate"])
+def test_row_scaled_b_ragged(M, N, K, out):
+    """Row-scaled B (a scale per column of D and 128-K block, as in Wgrad) on
+    the 1-CTA tiles (the first two shapes) and on the CTA-pair tiles (the
+    third: 18 x 9 tiles of 128 x 256, the last column of tiles half full),
+    with ragged M, every output element compared: FP32, BF16 and FP32 added
+    into D."""
+    torch, fp8bs = require_gpu()
+    a_bits = synth.normal_bf16((M, K), 1.0, 21, 1, outliers=True)
+    b_bits = synth.normal_bf16((N, K), 0.5, 21, 2)
+    aq, sa = fp8bs.quantize_act(to_dev_bf16(a_bits))
+    bq, sb = fp8bs.quantize_act(to_dev_bf16(b_bits))
+    qa, sa_ref = oracle.quantize_act_1x128(a_bits)
+    qb, sb_ref = oracle.quantize_act_1x128(b_bits)
+    Y, T = oracle.gemm_block_scaled(qa, sa_ref, qb, sb_ref, "row")
+    if out == "bf16":
+        d = fp8bs.gemm(aq, sa, bq, sb, sb_kind=fp8bs.SCALE_ROW1x128, out_dtype=torch.bfloat16)
+        assert fp8bs.fp8bs_get_device_status() == 0
+        check_bf16(to_host(d), Y, T, "row-scaled bf16")
+    elif out == "f32":
+        d = fp8bs.gemm(aq, sa, bq, sb, sb_kind=fp8bs.SCALE_ROW1x128, out_dtype=torch.float32)
+        assert fp8bs.fp8bs_get_device_status() == 0
+        check_f32(to_host(d), Y, T, "row-scaled f32")
+    else:
+        d0 = np.random.default_rng(M).standard_normal((M, N)).astype(np.float32)
+        d = to_dev(d0)
+        fp8bs.gemm(aq, sa, bq, sb, sb_kind=fp8bs.SCALE_ROW1x128, out=d, accumulate=True)
+        assert fp8bs.fp8bs_get_device_status() == 0
+        got = to_host(d).astype(np.float64)
+        assert np.all(np.abs(got - (d0 + Y)) <= 1e-5 * T + 2.0 ** -23 * np.abs(d0 + Y))
+
+
 def test_dense_fprop_full_size_sampled():
     """Y[4096,7168] = X[4096,7168] W[7168,7168]^T in BF16, as benchmarked."""
     x_bits, w_bits = synth.dense_fprop(0)
