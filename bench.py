@@ -462,46 +462,49 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                                     shape=f"grouped {E} experts, [{rows} x {H} x {I}], BF16 out")
         del aq, sa, bq, sb, d_in, w_dn
         # ---- the data movement around the expert GEMMs on one rank (the
-        # exchanges between ranks are the identity here): FP8 dispatch (pack
-        # the tokens' codes with row-major scales in send order, unpack into
-        # the experts' padded segments with kb-major scales) and BF16 combine
-        # (the expert outputs back in send order, then the gate-weighted sum)
+        # exchanges between ranks are the identity here): FP8 dispatch (pack:
+        # scatter the tokens' codes with row-major scales to their send rows;
+        # unpack: gather the received rows into the experts' padded segments
+        # with kb-major scales; one rank: scatter straight into the segments)
+        # and BF16 combine (the expert outputs back in send order, then the
+        # gate-weighted sum; one rank: the sum reading the expert rows in place)
         from fp8_fine_grained_fp8bs_gb300 import moe as moe_plan
         plan = moe_plan.MoePlan(choice, E, 1)
         recv = moe_plan.exchange_counts(plan)
         R, T_, nkb = plan.T * plan.k, plan.T, H // 128
         xq_tok, sx_tok = fp8bs.quantize_act(x_tok, pow2=True)
-        send_idx = torch.from_numpy(plan.send_token).to(dev)
+        send_pos = torch.from_numpy(plan.send_pos).to(dev)
         unpack_idx = torch.from_numpy(recv.unpack_idx).to(dev)
         back_idx = torch.from_numpy(recv.back_idx).to(dev)
-        send_pos = torch.from_numpy(plan.send_pos).to(dev)
+        local_pos = torch.from_numpy(recv.back_idx[plan.send_pos].astype(np.int32)).to(dev)
+        pad_rows = torch.from_numpy(recv.pad_rows).to(dev)
         gate_w = torch.from_numpy(synth.moe_gate_weights(seed=rank, tokens=T_, top_k=plan.k)).to(dev)
         q_send = torch.empty((R, H), dtype=torch.uint8, device=dev)
         s_send = torch.empty((R, nkb), dtype=torch.float32, device=dev)
         q_exp = torch.empty((recv.padded_rows, H), dtype=torch.uint8, device=dev)
         s_exp = torch.empty((nkb, recv.padded_rows), dtype=torch.float32, device=dev)
         row_b = H + 4 * nkb
-        ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, send_idx, R, q_send,
-                                                        s_send, fp8bs.SCALES_ROW_MAJOR, stream), stream, warmup, reps)
-        # each token's row is read from DRAM once (its k copies hit L2), each sent row written once
+        # each token's row is read once and written to its k send positions
+        ms = _time_ms(lambda: fp8bs.fp8bs_scatter_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, send_pos,
+                                                         plan.k, None, 0, R, q_send, s_send, fp8bs.SCALES_ROW_MAJOR,
+                                                         stream), stream, warmup, reps)
         out["moe_dispatch_pack"] = bw_line(T_ * row_b + R * row_b + 4 * R, ms,
-                                           shape=f"{R} (token, expert) rows of E4M3 [{H}] + {nkb} scales gathered "
-                                                 f"from {T_} tokens in send order")
+                                           shape=f"{T_} tokens of E4M3 [{H}] + {nkb} scales scattered to their "
+                                                 f"{R} (token, expert) send rows")
         ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(q_send, s_send, R, H, fp8bs.SCALES_ROW_MAJOR, unpack_idx,
                                                         recv.padded_rows, q_exp, s_exp, fp8bs.SCALES_KB_MAJOR, stream),
                       stream, warmup, reps)
         out["moe_dispatch_unpack"] = bw_line(R * row_b + recv.padded_rows * (row_b + 4), ms,
                                              shape=f"{R} received rows into {E} expert segments padded to 128 "
                                                    f"({recv.padded_rows} rows)")
-        direct_idx = torch.from_numpy(np.where(recv.unpack_idx >= 0,
-                                               plan.send_token[np.maximum(recv.unpack_idx, 0)], -1)
-                                      .astype(np.int32)).to(dev)
-        ms = _time_ms(lambda: fp8bs.fp8bs_gather_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, direct_idx,
-                                                        recv.padded_rows, q_exp, s_exp, fp8bs.SCALES_KB_MAJOR, stream),
-                      stream, warmup, reps)
-        out["moe_dispatch_local"] = bw_line(T_ * row_b + recv.padded_rows * (row_b + 4), ms,
-                                            shape=f"one rank: {T_} tokens straight into {E} expert segments padded "
-                                                  f"to 128 ({recv.padded_rows} rows)")
+        n_pad = int(recv.pad_rows.size)
+        ms = _time_ms(lambda: fp8bs.fp8bs_scatter_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, local_pos,
+                                                         plan.k, pad_rows, n_pad, recv.padded_rows, q_exp, s_exp,
+                                                         fp8bs.SCALES_KB_MAJOR, stream), stream, warmup, reps)
+        out["moe_dispatch_local"] = bw_line(T_ * row_b + recv.padded_rows * row_b + 4 * (R + n_pad), ms,
+                                            shape=f"one rank: {T_} tokens scattered straight into {E} expert "
+                                                  f"segments padded to 128 ({recv.padded_rows} rows, {n_pad} "
+                                                  f"zeroed)")
         y_back = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
         comb = torch.empty((T_, H), dtype=torch.bfloat16, device=dev)
         ms = _time_ms(lambda: fp8bs.fp8bs_gather_bf16_rows(y2, rows, H, back_idx, R, y_back, stream), stream, warmup,
@@ -512,12 +515,11 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                       warmup, reps)
         out["moe_combine"] = bw_line(R * H * 2 + T_ * H * 2 + 8 * R, ms,
                                      shape=f"{T_} tokens x top-{plan.k}: gate-weighted BF16 sum in FP32 -> BF16 [{H}]")
-        local_pos = torch.from_numpy(recv.back_idx[plan.send_pos].astype(np.int32)).to(dev)
         ms = _time_ms(lambda: fp8bs.fp8bs_moe_combine(y2, rows, H, local_pos, gate_w, T_, plan.k, comb, stream),
                       stream, warmup, reps)
         out["moe_combine_local"] = bw_line(R * H * 2 + T_ * H * 2 + 8 * R, ms,
                                            shape="one rank: the same sum reading the expert rows in place")
-        del y2, xq_tok, sx_tok, q_send, s_send, q_exp, s_exp, y_back, comb, direct_idx, local_pos
+        del y2, xq_tok, sx_tok, q_send, s_send, q_exp, s_exp, y_back, comb, local_pos, pad_rows
     if "pow2" in sections:
         # ---- power-of-two scales applied by the tensor core (UE8M0 block
         # scales of tcgen05.mma.kind::mxf8f6f4), next to the fold GEMM on the

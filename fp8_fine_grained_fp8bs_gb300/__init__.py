@@ -23,7 +23,8 @@ __all__ = [
     "Fp8bsError", "load_library", "build",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm", "fp8bs_grouped_gemm",
     "fp8bs_gemm_pow2", "fp8bs_grouped_gemm_pow2",
-    "fp8bs_gather_q_rows", "fp8bs_gather_bf16_rows", "fp8bs_moe_combine", "SCALES_KB_MAJOR", "SCALES_ROW_MAJOR",
+    "fp8bs_gather_q_rows", "fp8bs_scatter_q_rows", "fp8bs_gather_bf16_rows", "fp8bs_moe_combine", "SCALES_KB_MAJOR",
+    "SCALES_ROW_MAJOR",
     "fp8bs_quantize_act_ex", "fp8bs_quantize_weight_ex", "fp8bs_quantize_act_weight", "quantize_act_weight", "fp8bs_requant_1x128_to_128x1", "fp8bs_swiglu_quantize",
     "fp8bs_get_device_status", "fp8bs_set_wait_timeout_ms", "fp8bs_status_string", "fp8bs_selftest_wait_timeout",
     "fp8bs_diag_gemm_unpromoted", "diag_gemm_unpromoted",
@@ -67,6 +68,8 @@ _SIGNATURES = {
     "fp8bs_grouped_gemm_pow2": [_c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                                 _c_vp],
     "fp8bs_gather_q_rows": [_c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_vp, _c_i64, _c_vp, _c_vp, _c_int, _c_vp],
+    "fp8bs_scatter_q_rows": [_c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_vp, _c_int, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp,
+                             _c_int, _c_vp],
     "fp8bs_gather_bf16_rows": [_c_vp, _c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp],
     "fp8bs_moe_combine": [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp],
     "fp8bs_get_device_status": [_c_vp],
@@ -187,6 +190,14 @@ def fp8bs_gather_q_rows(q, s, rows_in, H, s_in_layout, idx, rows_out, q_out, s_o
     _check(load_library().fp8bs_gather_q_rows(_ptr(q), _ptr(s), rows_in, H, int(s_in_layout), _ptr(idx), rows_out,
                                               _ptr(q_out), _ptr(s_out), int(s_out_layout), _stream(stream)),
            "fp8bs_gather_q_rows")
+
+
+def fp8bs_scatter_q_rows(q, s, rows_in, H, s_in_layout, pos, k, zero_rows, n_zero, rows_out, q_out, s_out,
+                         s_out_layout, stream=None):
+    _check(load_library().fp8bs_scatter_q_rows(_ptr(q), _ptr(s), rows_in, H, int(s_in_layout), _ptr(pos), int(k),
+                                               _ptr(zero_rows), n_zero, rows_out, _ptr(q_out), _ptr(s_out),
+                                               int(s_out_layout), _stream(stream)),
+           "fp8bs_scatter_q_rows")
 
 
 def fp8bs_gather_bf16_rows(y, rows_in, N, idx, rows_out, out, stream=None):

@@ -288,6 +288,32 @@ int fp8bs_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64
                                                static_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_scatter_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, int s_in_layout,
+                         const int32_t* pos, int k, const int32_t* zero_rows, int64_t n_zero, int64_t rows_out,
+                         uint8_t* q_out, float* s_out, int s_out_layout, void* stream) {
+  if (rows_in < 0 || rows_out < 0 || H < 0 || n_zero < 0) return FP8BS_ERR_INVALID_ARG;
+  if (k < 1 || k > 64) return FP8BS_ERR_INVALID_ARG;
+  if ((s_in_layout != FP8BS_SCALES_KB_MAJOR && s_in_layout != FP8BS_SCALES_ROW_MAJOR) ||
+      (s_out_layout != FP8BS_SCALES_KB_MAJOR && s_out_layout != FP8BS_SCALES_ROW_MAJOR))
+    return FP8BS_ERR_INVALID_ARG;
+  if (H % 128 != 0) return FP8BS_ERR_SHAPE;
+  if (rows_in > ((int64_t(1) << 31) - 1) / k || rows_out > (int64_t(1) << 31) || n_zero > (int64_t(1) << 31) ||
+      H > (int64_t(1) << 24))
+    return FP8BS_ERR_SHAPE;
+  if (rows_out == 0 || H == 0 || (rows_in == 0 && n_zero == 0)) return FP8BS_OK;
+  if (q_out == nullptr || s_out == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (rows_in > 0 && (q == nullptr || s == nullptr || pos == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (n_zero > 0 && zero_rows == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(q_out)) return FP8BS_ERR_ALIGNMENT;
+  int sms = 0;
+  const int st = current_device(&sms);
+  if (st != FP8BS_OK) return st;
+  return from_cuda(fp8bs::launch_scatter_q_rows(q, s, rows_in, H, s_in_layout == FP8BS_SCALES_KB_MAJOR, pos, k,
+                                                zero_rows, n_zero, rows_out, q_out, s_out,
+                                                s_out_layout == FP8BS_SCALES_KB_MAJOR, sms,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_gather_bf16_rows(const void* y, int64_t rows_in, int64_t N, const int32_t* idx, int64_t rows_out,
                            void* out, void* stream) {
   if (rows_in < 0 || rows_out < 0 || N < 0) return FP8BS_ERR_INVALID_ARG;

@@ -78,6 +78,10 @@ cudaError_t gemm_mx_take_status(int* status);
 cudaError_t launch_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, bool s_in_kb_major,
                                  const int32_t* idx, int64_t rows_out, uint8_t* q_out, float* s_out,
                                  bool s_out_kb_major, int sm_count, cudaStream_t stream);
+cudaError_t launch_scatter_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, bool s_in_kb_major,
+                                  const int32_t* pos, int k, const int32_t* zero_rows, int64_t n_zero,
+                                  int64_t rows_out, uint8_t* q_out, float* s_out, bool s_out_kb_major, int sm_count,
+                                  cudaStream_t stream);
 cudaError_t launch_gather_bf16_rows(const uint16_t* y, int64_t rows_in, int64_t N, const int32_t* idx,
                                     int64_t rows_out, uint16_t* out, int sm_count, cudaStream_t stream);
 cudaError_t launch_moe_combine(const uint16_t* y, int64_t rows_y, int64_t N, const int32_t* idx, const float* w,

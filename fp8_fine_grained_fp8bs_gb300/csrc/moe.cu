@@ -10,6 +10,10 @@
 //     [rows][H/128], one contiguous record per row for an exchange);
 //     idx[i] < 0 gives a zero row with zero scales (the padding of an
 //     expert's segment to a multiple of 128 rows).
+//   * scatter_q_rows: the same movement from the sender's side: in row r
+//     goes to out rows pos[r][0..k), each read once and written k times
+//     (the gather form reads a row k times, from L2 at best); a second list
+//     names out rows to fill with zero codes and scales (padding).
 //   * gather_bf16_rows: out row i = in row idx[i] of a BF16 matrix (zeros
 //     for idx[i] < 0): the expert outputs put back in send order.
 //   * moe_combine: out[t] = BF16(sum_j w[t][j] * y[idx[t][j]]) with the
@@ -29,6 +33,7 @@ namespace {
 
 constexpr int kMoeThreads = 256;
 constexpr int kMoeWarps = kMoeThreads / 32;
+constexpr int kRowBatch = 4;  // 16-byte pieces per lane loaded before they are stored
 
 __global__ void __launch_bounds__(kMoeThreads) gather_q_rows_kernel(const uint8_t* __restrict__ q,
                                                                      const float* __restrict__ s, int64_t rows_in,
@@ -46,11 +51,70 @@ __global__ void __launch_bounds__(kMoeThreads) gather_q_rows_kernel(const uint8_
     const bool valid = src >= 0 && src < rows_in;
     const uint4* qi = reinterpret_cast<const uint4*>(q + (valid ? static_cast<int64_t>(src) : 0) * H);
     uint4* qo = reinterpret_cast<uint4*>(q_out + i * H);
-    for (int64_t v = lane; v < vec; v += 32) qo[v] = valid ? __ldg(qi + v) : make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t v0 = lane; v0 < vec; v0 += 32 * kRowBatch) {
+      uint4 d[kRowBatch];  // the batch's loads in flight together
+#pragma unroll
+      for (int u = 0; u < kRowBatch; ++u) {
+        const int64_t v = v0 + 32 * u;
+        d[u] = valid && v < vec ? __ldg(qi + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowBatch; ++u)
+        if (v0 + 32 * u < vec) qo[v0 + 32 * u] = d[u];
+    }
     for (int64_t kb = lane; kb < nkb; kb += 32) {
       float sv = 0.0f;
       if (valid) sv = __ldg(s + (s_in_kb_major ? kb * rows_in + src : static_cast<int64_t>(src) * nkb + kb));
       s_out[s_out_kb_major ? kb * rows_out + i : i * nkb + kb] = sv;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMoeThreads) scatter_q_rows_kernel(
+    const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t rows_in, int64_t H, int s_in_kb_major,
+    const int32_t* __restrict__ pos, int k, const int32_t* __restrict__ zero_rows, int64_t n_zero, int64_t rows_out,
+    uint8_t* __restrict__ q_out, float* __restrict__ s_out, int s_out_kb_major) {
+  griddep_launch_dependents();  // the grouped GEMM on the scattered rows may start its set-up
+  const int lane = threadIdx.x & 31;
+  const int64_t nkb = H / kGroup;
+  const int64_t vec = H / 16;
+  const int64_t items = rows_in + n_zero;  // source rows, then padding rows
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMoeWarps + (threadIdx.x >> 5); i < items;
+       i += static_cast<int64_t>(gridDim.x) * kMoeWarps) {
+    if (i >= rows_in) {
+      const int32_t dst = zero_rows[i - rows_in];
+      if (dst < 0 || dst >= rows_out) continue;
+      uint4* qo = reinterpret_cast<uint4*>(q_out + static_cast<int64_t>(dst) * H);
+      for (int64_t v = lane; v < vec; v += 32) qo[v] = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t kb = lane; kb < nkb; kb += 32)
+        s_out[s_out_kb_major ? kb * rows_out + dst : static_cast<int64_t>(dst) * nkb + kb] = 0.0f;
+      continue;
+    }
+    const int32_t* pr = pos + i * k;  // this row's destinations (the same address for every lane)
+    const uint4* qi = reinterpret_cast<const uint4*>(q + i * H);
+    for (int64_t v0 = lane; v0 < vec; v0 += 32 * kRowBatch) {
+      uint4 d[kRowBatch];
+#pragma unroll
+      for (int u = 0; u < kRowBatch; ++u) {
+        const int64_t v = v0 + 32 * u;
+        d[u] = v < vec ? __ldg(qi + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int32_t dst = __ldg(pr + j);
+        if (dst < 0 || dst >= rows_out) continue;
+        uint4* qo = reinterpret_cast<uint4*>(q_out + static_cast<int64_t>(dst) * H);
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u)
+          if (v0 + 32 * u < vec) qo[v0 + 32 * u] = d[u];
+      }
+    }
+    for (int64_t kb = lane; kb < nkb; kb += 32) {
+      const float sv = __ldg(s + (s_in_kb_major ? kb * rows_in + i : i * nkb + kb));
+      for (int j = 0; j < k; ++j) {
+        const int32_t dst = __ldg(pr + j);
+        if (dst < 0 || dst >= rows_out) continue;
+        s_out[s_out_kb_major ? kb * rows_out + dst : static_cast<int64_t>(dst) * nkb + kb] = sv;
+      }
     }
   }
 }
@@ -142,6 +206,18 @@ cudaError_t launch_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_
   if (rows_out <= 0) return cudaSuccess;
   gather_q_rows_kernel<<<grid_for_rows(rows_out, sm_count), kMoeThreads, 0, stream>>>(
       q, s, rows_in, H, s_in_kb_major ? 1 : 0, idx, rows_out, q_out, s_out, s_out_kb_major ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, bool s_in_kb_major,
+                                  const int32_t* pos, int k, const int32_t* zero_rows, int64_t n_zero,
+                                  int64_t rows_out, uint8_t* q_out, float* s_out, bool s_out_kb_major, int sm_count,
+                                  cudaStream_t stream) {
+  const int64_t items = rows_in + n_zero;
+  if (items <= 0 || rows_out <= 0) return cudaSuccess;
+  scatter_q_rows_kernel<<<grid_for_rows(items, sm_count), kMoeThreads, 0, stream>>>(
+      q, s, rows_in, H, s_in_kb_major ? 1 : 0, pos, k, zero_rows, n_zero, rows_out, q_out, s_out,
+      s_out_kb_major ? 1 : 0);
   return cudaGetLastError();
 }
 

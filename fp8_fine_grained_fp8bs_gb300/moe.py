@@ -25,12 +25,13 @@ e // (E/world), local index e % (E/world)).  One rank's routing is topk
     go back in the order the rows came.
 
 The plans are host index arithmetic.  The data movement runs in the CUDA
-library (fp8bs_gather_q_rows, fp8bs_gather_bf16_rows, fp8bs_moe_combine) and
-the exchanges in torch.distributed (NCCL between GPUs); with one rank there is
-no exchange, and dispatch and combine each take one launch that reads the
-tokens (or the expert rows) in place through the composed indices.  The movement and exchange steps
-are parameters of dispatch() and combine() so that the exchange protocol can
-be exercised with other implementations of them.
+library (fp8bs_scatter_q_rows, fp8bs_gather_q_rows, fp8bs_gather_bf16_rows,
+fp8bs_moe_combine) and the exchanges in torch.distributed (NCCL between
+GPUs); with one rank there is no exchange, and dispatch and combine each take
+one launch that moves the tokens (or the expert rows) through the composed
+indices.  The movement and exchange steps are parameters of dispatch() and
+combine() so that the exchange protocol can be exercised with other
+implementations of them.
 """
 from __future__ import annotations
 
@@ -96,6 +97,7 @@ class RecvPlan:
                 pos += n
         self.unpack_idx = unpack     # padded expert row -> received row (-1: zero padding)
         self.back_idx = back         # received row -> its padded expert row
+        self.pad_rows = np.nonzero(unpack < 0)[0].astype(np.int32)   # the padding rows
 
 
 def exchange_counts(plan: MoePlan, all_to_all=None, make_tensor=None) -> RecvPlan:
@@ -135,6 +137,23 @@ def _kernel_gather_q(q, s, s_in_kb, idx, s_out_kb):
     return q_out, s_out
 
 
+def _kernel_scatter_q(q, s, s_in_kb, pos, zero_rows, rows_out, s_out_kb):
+    """Library row scatter of FP8 codes and scales (fp8bs_scatter_q_rows):
+    row r goes to out rows pos[r, :]; zero_rows are filled with zeros."""
+    import torch
+    from . import fp8bs_scatter_q_rows, SCALES_KB_MAJOR, SCALES_ROW_MAJOR
+    rows_in, H = q.shape
+    k = int(pos.shape[1])
+    q_out = torch.empty((rows_out, H), dtype=torch.uint8, device=q.device)
+    s_out = torch.empty((H // 128, rows_out) if s_out_kb else (rows_out, H // 128), dtype=torch.float32,
+                        device=q.device)
+    n_zero = int(zero_rows.numel()) if zero_rows is not None else 0
+    fp8bs_scatter_q_rows(q, s, rows_in, H, SCALES_KB_MAJOR if s_in_kb else SCALES_ROW_MAJOR, pos, k,
+                         zero_rows if n_zero else None, n_zero, rows_out, q_out, s_out,
+                         SCALES_KB_MAJOR if s_out_kb else SCALES_ROW_MAJOR)
+    return q_out, s_out
+
+
 def _kernel_gather_bf16(y, idx):
     import torch
     from . import fp8bs_gather_bf16_rows
@@ -153,21 +172,23 @@ def _kernel_combine(y, idx, w):
     return out
 
 
-def dispatch(xq, sx, plan: MoePlan, recv: RecvPlan, gather_q=None, all_to_all=None, to_index=None):
+def dispatch(xq, sx, plan: MoePlan, recv: RecvPlan, gather_q=None, scatter_q=None, all_to_all=None, to_index=None):
     """FP8 dispatch: xq [T, H] E4M3 codes and sx [H/128, T] (kb-major) scales of
     this rank's tokens -> the local experts' rows (q [padded_rows, H], s
     [H/128, padded_rows] kb-major), padded segments at recv.offsets.
 
-    Pack (rows in send order, scales row-major so each row's scales travel
-    with it), exchange codes and scales, unpack into the expert segments."""
+    Pack (each token row read once and written to its send positions, scales
+    row-major so each row's scales travel with it), exchange codes and scales,
+    unpack into the expert segments.  With one rank the tokens are scattered
+    straight into the segments (send position -> expert row composed) and the
+    padding rows zeroed in the same launch."""
+    sc = scatter_q or _kernel_scatter_q
     g = gather_q or _kernel_gather_q
     ix = to_index or (lambda a: _idx(a, xq.device))
     if plan.world == 1:
-        # no exchange: the expert segments gather the tokens directly (the
-        # composition of the pack and unpack indices; -1 stays padding)
-        direct = np.where(recv.unpack_idx >= 0, plan.send_token[np.maximum(recv.unpack_idx, 0)], -1)
-        return g(xq, sx, True, ix(direct), True)
-    send_q, send_s = g(xq, sx, True, ix(plan.send_token), False)
+        return sc(xq, sx, True, ix(recv.back_idx[plan.send_pos]), ix(recv.pad_rows), recv.padded_rows, True)
+    R = int(plan.send_counts.sum())
+    send_q, send_s = sc(xq, sx, True, ix(plan.send_pos), None, R, False)
     recv_q = send_q.new_empty((recv.rows, send_q.shape[1]))
     recv_s = send_s.new_empty((recv.rows, send_s.shape[1]))
     (all_to_all or _a2a)(recv_q, send_q, recv.recv_per_src, plan.send_counts)

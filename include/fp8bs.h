@@ -305,6 +305,29 @@ int fp8bs_gather_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64
                         void* stream);
 
 /*
+ * Row scatter of FP8 codes with their 1x128 scales: the dispatch written from
+ * the sender's side, each token row read once and written to each of its k
+ * destinations (§3.3.3 "low-precision communication", as fp8bs_gather_q_rows):
+ *
+ *   for r < rows_in, j < k:  if 0 <= pos[r*k + j] < rows_out, out row
+ *     pos[r*k + j] = q[r][:] with the scales of row r;
+ *   for i < n_zero:  if 0 <= zero_rows[i] < rows_out, out row zero_rows[i] =
+ *     zero codes with zero scales (the padding of an expert's segment).
+ *
+ *   q      [rows_in][H] E4M3 codes.  s: float32 scales in s_in_layout.   (in)
+ *   pos    DEVICE int32 [rows_in][k]; zero_rows DEVICE int32 [n_zero]
+ *          (NULL allowed when n_zero == 0).                               (in)
+ *   q_out  [rows_out][H] E4M3.  s_out: float32 scales in s_out_layout.   (out)
+ * Out rows named by neither list are left as they are; a row named more than
+ * once gets one of its writes, which one is unspecified.
+ * Rules: H % 128 == 0; 1 <= k <= 64; n_zero >= 0; q, q_out 16-byte aligned;
+ * the layouts are fp8bs_scale_layout values (FP8BS_ERR_INVALID_ARG otherwise).
+ */
+int fp8bs_scatter_q_rows(const uint8_t* q, const float* s, int64_t rows_in, int64_t H, int s_in_layout,
+                         const int32_t* pos, int k, const int32_t* zero_rows, int64_t n_zero, int64_t rows_out,
+                         uint8_t* q_out, float* s_out, int s_out_layout, void* stream);
+
+/*
  * Row gather of a BF16 matrix (the expert outputs put back in send order for
  * the combine, which §3.3.3 keeps in BF16):
  *   out[i][:] = y[idx[i]][:], zeros where idx[i] < 0 or >= rows_in.

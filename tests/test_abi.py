@@ -132,6 +132,20 @@ def test_moe_row_kernels_argument_errors(lib):
     assert cb(FAKE, 10, 16, FAKE, FAKE, 4, 65, FAKE, None) == 1                # k > 64
     assert cb(FAKE, 10, 12, FAKE, FAKE, 4, 2, FAKE, None) == 2
     assert cb(FAKE, 10, 16, None, FAKE, 4, 2, FAKE, None) == 1
+    sq = lib.fp8bs_scatter_q_rows
+    #        q     s     rows_in H   lay pos   k  zero  nz rows_out q_out s_out lay
+    assert sq(FAKE, FAKE, 10, 100, 0, FAKE, 2, None, 0, 20, FAKE, FAKE, 1, None) == 2    # H % 128
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 0, None, 0, 20, FAKE, FAKE, 1, None) == 1    # k < 1
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 65, None, 0, 20, FAKE, FAKE, 1, None) == 1   # k > 64
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 2, None, -1, 20, FAKE, FAKE, 1, None) == 1   # n_zero < 0
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 2, None, 3, 20, FAKE, FAKE, 1, None) == 1    # zero list missing
+    assert sq(FAKE, FAKE, 10, 128, 3, FAKE, 2, None, 0, 20, FAKE, FAKE, 1, None) == 1    # unknown layout
+    assert sq(FAKE, FAKE, 10, 128, 0, None, 2, None, 0, 20, FAKE, FAKE, 1, None) == 1    # no positions
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 2, None, 0, 20, FAKE + 4, FAKE, 1, None) == 3
+    assert sq(FAKE, FAKE, 2 ** 30, 128, 0, FAKE, 4, None, 0, 20, FAKE, FAKE, 1, None) == 2  # rows_in * k >= 2^31
+    assert sq(FAKE, FAKE, 10, 128, 0, FAKE, 2, None, 0, 20, None, None, 0, None) == 1       # no output buffers
+    assert sq(None, None, 0, 128, 0, None, 2, None, 0, 20, None, None, 0, None) == 0       # nothing to move
+    assert sq(None, None, 0, 128, 0, None, 2, None, 0, 0, None, None, 0, None) == 0        # empty: no-op
 
 
 def test_quantize_act_weight_argument_errors(lib):

@@ -2,10 +2,10 @@
 
 DeepSeek-V3 §3.3.3, low-precision communication: the dispatched rows are
 E4M3 codes with their power-of-two 1x128 scales, the combine sums BF16
-expert outputs with the gate weights.  The row gathers must move codes,
-scales and BF16 values bit for bit (numpy computes the expected rows from
-the same index arrays); the combine must be within 1 BF16 ulp of the oracle's
-correctly rounded weighted sum.  With one rank the exchanges are the
+expert outputs with the gate weights.  The row gathers and the scatter must
+move codes, scales and BF16 values bit for bit (numpy computes the expected
+rows from the same index arrays); the combine must be within 1 BF16 ulp of
+the oracle's correctly rounded weighted sum.  With one rank the exchanges are the
 identity, so dispatch -> grouped GEMM -> combine runs whole here and is
 checked against the oracle.
 """
@@ -47,6 +47,45 @@ def test_gather_q_rows(s_in_kb, s_out_kb):
     got_s = to_host(s_out)
     got_s = got_s.T if s_out_kb else got_s
     assert np.array_equal(got_s.view(np.uint32), _np_rows(s, idx).view(np.uint32))
+
+
+@pytest.mark.parametrize("s_in_kb", [True, False])
+@pytest.mark.parametrize("s_out_kb", [True, False])
+def test_scatter_q_rows(s_in_kb, s_out_kb):
+    """Each input row to its k destinations, listed rows zeroed, the rest of
+    the output untouched; destinations out of range are skipped."""
+    torch, fp8bs = require_gpu()
+    rows_in, H, k, rows_out = 300, 640, 3, 1000
+    rng = np.random.default_rng(3)
+    q = rng.integers(0, 256, (rows_in, H), dtype=np.uint8)
+    s = rng.standard_normal((rows_in, H // 128)).astype(np.float32)
+    perm = rng.permutation(rows_out).astype(np.int32)
+    pos = perm[:rows_in * k].reshape(rows_in, k).copy()
+    pos[::17, 1] = -1                   # skipped
+    pos[::23, 2] = rows_out + 5         # out of range: skipped
+    zero_rows = np.concatenate([perm[rows_in * k:rows_in * k + 60], [-1, rows_out]]).astype(np.int32)
+    untouched = perm[rows_in * k + 60:]
+    q_out = torch.full((rows_out, H), 0x5A, dtype=torch.uint8, device="cuda:0")
+    s_out = torch.full((H // 128, rows_out) if s_out_kb else (rows_out, H // 128), 7.0, dtype=torch.float32,
+                       device="cuda:0")
+    s_dev = to_dev(np.ascontiguousarray(s.T) if s_in_kb else s)
+    fp8bs.fp8bs_scatter_q_rows(to_dev(q), s_dev, rows_in, H, 0 if s_in_kb else 1, to_dev(pos), k,
+                               to_dev(zero_rows), len(zero_rows), rows_out, q_out, s_out, 0 if s_out_kb else 1)
+    torch.cuda.synchronize()
+    exp_q = np.full((rows_out, H), 0x5A, np.uint8)
+    exp_s = np.full((rows_out, H // 128), 7.0, np.float32)
+    for r in range(rows_in):
+        for d in pos[r]:
+            if 0 <= d < rows_out:
+                exp_q[d], exp_s[d] = q[r], s[r]
+    for d in zero_rows:
+        if 0 <= d < rows_out:
+            exp_q[d], exp_s[d] = 0, 0.0
+    got_s = to_host(s_out)
+    got_s = got_s.T if s_out_kb else got_s
+    assert np.array_equal(to_host(q_out), exp_q)
+    assert np.array_equal(got_s.view(np.uint32), exp_s.view(np.uint32))
+    assert np.all(to_host(q_out)[untouched] == 0x5A)
 
 
 def test_gather_bf16_rows():

@@ -9,7 +9,7 @@ plans the exchange (fp8_fine_grained_fp8bs_gb300.moe), exchanges the counts,
 the E4M3 codes with their scales, and the BF16 expert outputs with gloo
 all-to-alls, and computes the expert GEMMs, SwiGLU and combine with the
 oracle; the row copies around the exchanges are numpy here (the library's
-gather kernels are checked on the GPU).  Every row's arithmetic depends on
+scatter and gather kernels are checked on the GPU).  Every row's arithmetic depends on
 that row only, so the two ranks' outputs must equal the single-process
 layer over all tokens bit for bit.
 """
@@ -40,6 +40,25 @@ def _np_gather_q(q, s, s_in_kb, idx, s_out_kb):
     so = np.zeros((len(idx), rows.shape[1]), np.float32)
     qo[ok] = qn[idx[ok]]
     so[ok] = rows[idx[ok]]
+    return torch.from_numpy(qo), torch.from_numpy(np.ascontiguousarray(so.T) if s_out_kb else so)
+
+
+def _np_scatter_q(q, s, s_in_kb, pos, zero_rows, rows_out, s_out_kb):
+    qn, sn = q.numpy(), s.numpy()
+    rows = sn.T if s_in_kb else sn
+    qo = np.zeros((rows_out, qn.shape[1]), np.uint8)
+    so = np.zeros((rows_out, rows.shape[1]), np.float32)
+    written = np.zeros(rows_out, np.int64)
+    for r in range(qn.shape[0]):
+        for d in pos[r]:
+            if 0 <= d < rows_out:
+                qo[d] = qn[r]
+                so[d] = rows[r]
+                written[d] += 1
+    if zero_rows is not None:
+        written[np.asarray(zero_rows)] += 1
+    # the planner names every out row exactly once (a token row or padding)
+    assert np.all(written == 1), np.bincount(written)
     return torch.from_numpy(qo), torch.from_numpy(np.ascontiguousarray(so.T) if s_out_kb else so)
 
 
@@ -95,7 +114,7 @@ def _layer(x, topk, gw, world, rank, w):
     plan = moe.MoePlan(topk, E, world)
     recv = moe.exchange_counts(plan)
     q_exp, s_exp = moe.dispatch(torch.from_numpy(q), torch.from_numpy(np.ascontiguousarray(s.T)), plan, recv,
-                                gather_q=_np_gather_q, to_index=lambda a: a)
+                                gather_q=_np_gather_q, scatter_q=_np_scatter_q, to_index=lambda a: a)
     ids = rank * plan.epr + np.arange(plan.epr)
     y = _experts(q_exp.numpy(), s_exp.numpy(), recv.offsets, ids, w)
     out = moe.combine(torch.from_numpy(y), gw, plan, recv, gather_bf16=_np_gather_bf16, combine_rows=_np_combine,
