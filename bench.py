@@ -838,6 +838,10 @@ def main():
         "peak_source": f"{peak_src}: bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)",
         "hw_rate_peak": hw_peak, "frac_of_hw_rate": gemm_tflops / hw_peak,
         "hw_rate_source": f"{sms} SMs x 16384 FP8 FLOP/clk/SM x {max_mhz:g} MHz (maximum SM clock)"}
+    if clocks.get("sm_mhz"):
+        hw_med = hw_fp8_peak_tflops(sms, clocks["sm_mhz"])
+        line["roofline"]["hw_rate_peak_median_clock"] = hw_med
+        line["roofline"]["frac_of_hw_rate_median_clock"] = gemm_tflops / hw_med
     line["gemm"] = {"tflops": gemm_tflops, "ms": gemm_ms, "frac_of_fp8_peak": gemm_tflops / fp8_peak,
                     "frac_of_hw_rate": gemm_tflops / hw_peak}
     line["quantize_roofline"] = {
