@@ -519,7 +519,42 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
                       stream, warmup, reps)
         out["moe_combine_local"] = bw_line(R * H * 2 + T_ * H * 2 + 8 * R, ms,
                                            shape="one rank: the same sum reading the expert rows in place")
-        del y2, xq_tok, sx_tok, q_send, s_send, q_exp, s_exp, y_back, comb, local_pos, pad_rows
+        # ---- the whole MoE layer on one rank, launched back to back as a user
+        # runs it: FP8 dispatch (scatter into the padded expert segments), the
+        # gate/up grouped GEMM, the fused SwiGLU quantise, the down grouped GEMM
+        # and the BF16 combine; TFLOP/s of the two GEMMs' real-row flops
+        del y_back
+        w_gu = (torch.randn((E * 2 * I, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        gq, gs = fp8bs.quantize_weight(w_gu)
+        del w_gu
+        w_dn = (torch.randn((E * H, I), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        dq, ds = fp8bs.quantize_weight(w_dn)
+        del w_dn
+        gq, gs = gq.view(E, 2 * I, H), gs.view(E, 2 * I // 128, H // 128)
+        dq, ds = dq.view(E, H, I), ds.view(E, H // 128, I // 128)
+        seg = torch.from_numpy(recv.offsets).to(dev)
+        h1 = torch.empty((recv.padded_rows, 2 * I), dtype=torch.bfloat16, device=dev)
+        hq = torch.empty((recv.padded_rows, I), dtype=torch.uint8, device=dev)
+        hs = torch.empty((I // 128, recv.padded_rows), dtype=torch.float32, device=dev)
+
+        def moe_layer():
+            fp8bs.fp8bs_scatter_q_rows(xq_tok, sx_tok, T_, H, fp8bs.SCALES_KB_MAJOR, local_pos, plan.k, pad_rows,
+                                       n_pad, recv.padded_rows, q_exp, s_exp, fp8bs.SCALES_KB_MAJOR, stream)
+            fp8bs.fp8bs_grouped_gemm(q_exp, s_exp, recv.padded_rows, seg, E, gq, gs, h1, fp8bs.OUT_BF16, 2 * I, H,
+                                     stream)
+            fp8bs.fp8bs_swiglu_quantize(h1, recv.padded_rows, I, 2 * I, hq, hs, fp8bs.SCALE_ABSMAX, stream)
+            fp8bs.fp8bs_grouped_gemm(hq, hs, recv.padded_rows, seg, E, dq, ds, y2, fp8bs.OUT_BF16, H, I, stream)
+            fp8bs.fp8bs_moe_combine(y2, recv.padded_rows, H, local_pos, gate_w, T_, plan.k, comb, stream)
+
+        ms = _time_ms(moe_layer, stream, warmup, reps)
+        if fp8bs.fp8bs_get_device_status(stream) != 0:
+            raise RuntimeError("device status after the MoE layer")
+        out["moe_layer"] = gemm_line(2.0 * R * (2 * I * H + H * I), ms, rows=recv.padded_rows, real_rows=R,
+                                     shape=f"one rank, {T_} tokens x top-{plan.k} of {E} experts, hidden {H}, "
+                                           f"expert {I}: dispatch, gate/up GEMM, SwiGLU quantise, down GEMM, "
+                                           "combine (5 launches)")
+        out["moe_layer"]["launches"] = 5
+        del y2, xq_tok, sx_tok, q_send, s_send, q_exp, s_exp, comb, local_pos, pad_rows, gq, gs, dq, ds, h1, hq, hs
     if "pow2" in sections:
         # ---- power-of-two scales applied by the tensor core (UE8M0 block
         # scales of tcgen05.mma.kind::mxf8f6f4), next to the fold GEMM on the
