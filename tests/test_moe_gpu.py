@@ -88,6 +88,37 @@ def test_scatter_q_rows(s_in_kb, s_out_kb):
     assert np.all(to_host(q_out)[untouched] == 0x5A)
 
 
+def test_scatter_q_rows_edge_cases():
+    """k = 1 (a permutation), no source rows with padding rows only, and a
+    single 128-column group."""
+    torch, fp8bs = require_gpu()
+    H = 128
+    rng = np.random.default_rng(4)
+    q = rng.integers(0, 256, (64, H), dtype=np.uint8)
+    s = rng.standard_normal((64, 1)).astype(np.float32)
+    pos = rng.permutation(64).astype(np.int32).reshape(64, 1)
+    q_out = torch.empty((64, H), dtype=torch.uint8, device="cuda:0")
+    s_out = torch.empty((1, 64), dtype=torch.float32, device="cuda:0")
+    fp8bs.fp8bs_scatter_q_rows(to_dev(q), to_dev(s), 64, H, 1, to_dev(pos), 1, None, 0, 64, q_out, s_out, 0)
+    torch.cuda.synchronize()
+    exp_q = np.empty_like(q)
+    exp_q[pos[:, 0]] = q
+    exp_s = np.empty(64, np.float32)
+    exp_s[pos[:, 0]] = s[:, 0]
+    assert np.array_equal(to_host(q_out), exp_q)
+    assert np.array_equal(to_host(s_out)[0].view(np.uint32), exp_s.view(np.uint32))
+    # only padding rows: rows 3 and 17 zeroed, the rest untouched
+    q_out.fill_(0x33)
+    s_out.fill_(2.0)
+    fp8bs.fp8bs_scatter_q_rows(None, None, 0, H, 0, None, 1, to_dev(np.array([3, 17], np.int32)), 2, 64, q_out,
+                               s_out, 0)
+    torch.cuda.synchronize()
+    got_q, got_s = to_host(q_out), to_host(s_out)[0]
+    assert np.all(got_q[[3, 17]] == 0) and np.all(got_s[[3, 17]] == 0.0)
+    assert np.all(np.delete(got_q, [3, 17], axis=0) == 0x33) and np.all(np.delete(got_s, [3, 17]) == 2.0)
+    assert fp8bs.fp8bs_get_device_status() == 0
+
+
 def test_gather_bf16_rows():
     torch, fp8bs = require_gpu()
     y = synth.normal_bf16((250, 1032), 2.0, 3, 1)
@@ -99,7 +130,7 @@ def test_gather_bf16_rows():
     assert np.array_equal(got, _np_rows(y, idx))
 
 
-@pytest.mark.parametrize("k", [1, 2, 8])
+@pytest.mark.parametrize("k", [1, 2, 8, 13])
 def test_combine_vs_oracle(k):
     torch, fp8bs = require_gpu()
     R, N, T = 700, 2048, 300
