@@ -632,7 +632,7 @@ def measure_workloads(fp8bs, synth, dev, stream, rank: int, fp8_peak: float, hbm
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="fp8bs", choices=["fp8bs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
