@@ -642,7 +642,7 @@ cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int
                          const uint16_t* w = nullptr, int64_t ldw = 0, const TileParams* pw = nullptr) {
   const int64_t ntiles = p.nrb * p.nkb + (pw != nullptr ? pw->nrb * pw->nkb : 0);
   if (ntiles <= 0) return cudaSuccess;
-  CUtensorMap map, map_w;
+  CUtensorMap map{}, map_w{};
   if (p.nrb > 0 &&
       !encode_bf16_tiles(&map, x, p.rows, static_cast<int64_t>(p.nkb) * kGroup, ld, QCfg<kMode>::kRowLayout))
     return cudaErrorInvalidValue;
