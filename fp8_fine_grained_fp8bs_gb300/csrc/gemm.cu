@@ -122,23 +122,6 @@ __device__ __forceinline__ void fold_block(float2* acc, const uint32_t (&p)[32],
     acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), s2, acc[j]);
 }
 
-// Row-scaled B in the fragment layout of tcgen05.ld.16x256b: p holds, for
-// 8-column groups g = 0..3, columns 8g + 2(lane % 4) + {0, 1} of two rows
-// (registers 4g, 4g+1 of the first, 4g+2, 4g+3 of the second, 8 rows
-// further); acc[2g + j] += p * (s_a[j] * s_b of the column pair g).
-__device__ __forceinline__ void fold_frag(float2* acc, const uint32_t (&p)[16], float sa0, float sa1,
-                                          const float2* sb) {
-  const float2 a0 = make_float2(sa0, sa0);
-  const float2 a1 = make_float2(sa1, sa1);
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    acc[2 * g] = __ffma2_rn(make_float2(__uint_as_float(p[4 * g]), __uint_as_float(p[4 * g + 1])),
-                            __fmul2_rn(a0, sb[g]), acc[2 * g]);
-    acc[2 * g + 1] = __ffma2_rn(make_float2(__uint_as_float(p[4 * g + 2]), __uint_as_float(p[4 * g + 3])),
-                                __fmul2_rn(a1, sb[g]), acc[2 * g + 1]);
-  }
-}
-
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_gemm_status, 0, code); }
 
 template <int BN, bool kRowScale, bool kGrouped, bool kPair>
@@ -439,37 +422,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Per-column scales: the partial is read in the fragment layout of
           // tcgen05.ld.16x256b, where a thread holds 8 of every 32 columns
           // (of 4 rows), so it needs a quarter of the column scales a
-          // row-per-thread layout needs: per 32-column chunk 4 pairs, loaded
+          // row-per-thread layout needs: per 64-column chunk 8 pairs, loaded
           // one chunk ahead (the first chunk's and the 4 row scales before
-          // the wait for the partial).
+          // the wait for the partial).  Pieces of 16 lanes x 64 columns (32
+          // registers) take half the loads of 32-column ones (3% faster).
           float sa4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) sa4[i] = scs[quarter * 32 + 8 * i + (lane >> 2)];
           const float* scol = scs + kBlockM + colhalf * C::kColsPerThread + 2 * (lane & 3);
-          float2 sbc[2][4];
+          float2 sbc[2][8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sbc[0][i] = *reinterpret_cast<const float2*>(scol + 8 * i);
+          for (int i = 0; i < 8; ++i) sbc[0][i] = *reinterpret_cast<const float2*>(scol + 8 * i);
           if (!mbar_wait(&t_full[buf], tphase, p.timeout_ns)) { live = false; break; }
           tc_fence_after_sync();
           const uint32_t tcol = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN +
                                 colhalf * C::kColsPerThread;
-          // pieces (32-column chunk c, 16-lane half h), chunk-major, the next
+          // pieces (64-column chunk c, 16-lane half h), chunk-major, the next
           // piece's load in flight while the current one is folded
-          constexpr int kFrag = 2 * C::kChunks;
-          uint32_t fr[2][16];
-          tmem_ld16x256b_x4(tcol, fr[0]);
+          constexpr int kC64 = C::kChunks / 2;
+          constexpr int kFrag = 2 * kC64;
+          uint32_t fr[2][32];
+          tmem_ld16x256b_x8(tcol, fr[0]);
           tmem_wait_ld(fr[0]);
 #pragma unroll
           for (int f = 0; f < kFrag; ++f) {
             const int h = f & 1, c = f >> 1;
-            if (h == 0 && c + 1 < C::kChunks) {
+            if (h == 0 && c + 1 < kC64) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                sbc[(c + 1) & 1][i] = *reinterpret_cast<const float2*>(scol + 32 * (c + 1) + 8 * i);
+              for (int i = 0; i < 8; ++i)
+                sbc[(c + 1) & 1][i] = *reinterpret_cast<const float2*>(scol + 64 * (c + 1) + 8 * i);
             }
             if (f + 1 < kFrag) {
               const int nh = (f + 1) & 1, nc = (f + 1) >> 1;
-              tmem_ld16x256b_x4(tcol + (static_cast<uint32_t>(16 * nh) << 16) + 32 * nc, fr[(f + 1) & 1]);
+              tmem_ld16x256b_x8(tcol + (static_cast<uint32_t>(16 * nh) << 16) + 64 * nc, fr[(f + 1) & 1]);
             } else {
               tc_fence_before_sync();
               __syncwarp();
@@ -480,7 +465,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mbar_arrive(&t_empty[buf]);
               }
             }
-            fold_frag(acc2 + (h * C::kChunks + c) * 8, fr[f & 1], sa4[2 * h], sa4[2 * h + 1], sbc[c & 1]);
+            {
+              const uint32_t (&pp)[32] = fr[f & 1];
+              const float2 a0 = make_float2(sa4[2 * h], sa4[2 * h]);
+              const float2 a1 = make_float2(sa4[2 * h + 1], sa4[2 * h + 1]);
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const int cc = 2 * c + (g >> 2), gg = g & 3;
+                float2* ac = acc2 + ((h * C::kChunks + cc) * 4 + gg) * 2;
+                ac[0] = __ffma2_rn(make_float2(__uint_as_float(pp[4 * g]), __uint_as_float(pp[4 * g + 1])),
+                                   __fmul2_rn(a0, sbc[c & 1][g]), ac[0]);
+                ac[1] = __ffma2_rn(make_float2(__uint_as_float(pp[4 * g + 2]), __uint_as_float(pp[4 * g + 3])),
+                                   __fmul2_rn(a1, sbc[c & 1][g]), ac[1]);
+              }
+            }
             if (f + 1 < kFrag) tmem_wait_ld(fr[(f + 1) & 1]);
           }
         } else {
