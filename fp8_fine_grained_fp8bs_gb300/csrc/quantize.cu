@@ -188,6 +188,33 @@ __device__ __forceinline__ uint32_t quant2_exact(uint32_t w, float s) {
   return e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s), __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
 }
 
+// The BF16 pair w (low half first) widened to float32 and negated: -x is
+// what quant_pair_nx takes.
+__device__ __forceinline__ float2 neg_widen(uint32_t w) {
+  return make_float2(__uint_as_float((w << 16) ^ 0x80000000u), __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u));
+}
+
+// Codes of a value pair given as nx = -x, with a divisor per half: s2 the
+// scales, ny2 = -RN(1/s).  The same Markstein quotient as quant_pair with
+// the signs moved: q0 = RN(nx * ny), r = RN(s q0 + nx) = -(x - s q0)
+// (exact), q1 = RN(q0 + r * ny).  In this form a zero input keeps its sign
+// (x = -0: q0 = -0, r = +0, q1 = -0 + -0 = -0), so no sign restoration
+// follows; every other input gives the same q1 as quant_pair.
+__device__ __forceinline__ uint32_t quant_pair_nx(float2 nx, float2 ny2, float2 s2) {
+  const float2 q0 = __fmul2_rn(nx, ny2);
+  const float2 r = __ffma2_rn(q0, s2, nx);
+  const float2 q1 = __ffma2_rn(r, ny2, q0);
+  return e4m3x2(q1.x, q1.y);
+}
+
+// Codes of the BF16 pair w through IEEE divisions, a scale per half (a
+// zero scale gives a zero code).
+__device__ __forceinline__ uint32_t quant2_exact_pair(uint32_t w, float s0, float s1) {
+  const float a = s0 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w << 16), s0);
+  const float b = s1 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s1);
+  return e4m3x2(a, b);
+}
+
 // Eight consecutive values of one group -> eight codes (byte i = value i).
 __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d) {
   if (!d.fast)
@@ -197,6 +224,11 @@ __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d) {
   const uint32_t c0 = quant_pair(v.x, y2, ns2), c1 = quant_pair(v.y, y2, ns2);
   const uint32_t c2 = quant_pair(v.z, y2, ns2), c3 = quant_pair(v.w, y2, ns2);
   return make_uint2(__byte_perm(c0, c1, 0x5410) | signs4(v.x, v.y), __byte_perm(c2, c3, 0x5410) | signs4(v.z, v.w));
+}
+
+// Word k (0..3) of a 16-byte vector.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
 // Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
@@ -278,8 +310,9 @@ struct QShared {
   DivTable tab;
   uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
   uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
-  float2 rowdiv[kGroup];                               // dual: per row (s, RN(1/s)); y < 0: exact path
-  float2 coldiv[kGroup];                               // dual: per column, the same
+  float2 rowdiv[kGroup];                               // dual: per row (s, -RN(1/s))
+  float col_s[kGroup];                                 // dual: per column s
+  float col_ny[kGroup];                                // dual: per column -RN(1/s)
 };
 
 template <int kMode>
@@ -545,36 +578,27 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       }
       // one divisor per row, computed by one thread of the row's half-warp
       // and shared through shared memory with the other fifteen
+      bool fast = true;  // this thread's row or column divisor takes the quotient path
       if (c < 8) {
         uint32_t a16 = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (j == c) a16 = (j & 1) ? (am[j >> 1] >> 16) : (am[j >> 1] & 0xFFFFu);
         const Divisor d = group_divisor(S.tab, a16, p.pow2 != 0);
-        S.rowdiv[8 * g + c] = make_float2(d.s, d.fast ? d.y : -1.0f);
+        S.rowdiv[8 * g + c] = make_float2(d.s, -d.y);
+        fast = d.fast;
         p.s[static_cast<int64_t>(kb) * p.rows + r0 + c] = d.s;
       }
-      // 128x1 groups: transpose the 8x8 sub-block (column i of the tile
-      // chunk becomes vector i: rows 8g .. 8g+7 of that column), reduce the
-      // column maxima over the 16 row groups, then quantise every column
-      // vector like a row chunk; its 8 codes are 8 consecutive bytes of X^T.
-      uint4 vt[8];
+      // 128x1 groups: word k of the thread's eight rows holds columns
+      // 8c+2k and 8c+2k+1, so the column maxima over the sub-block are
+      // running maxima over the rows; the two row groups of a warp meet by
+      // one shuffle and the 16 warps' partial maxima in shared memory.
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint32_t lo[4], hi[4];
+        uint32_t m = word_of(v[0], k);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t a = k == 0 ? v[2 * m].x : k == 1 ? v[2 * m].y : k == 2 ? v[2 * m].z : v[2 * m].w;
-          const uint32_t b = k == 0 ? v[2 * m + 1].x : k == 1 ? v[2 * m + 1].y : k == 2 ? v[2 * m + 1].z : v[2 * m + 1].w;
-          lo[m] = __byte_perm(a, b, 0x5410);
-          hi[m] = __byte_perm(a, b, 0x7632);
-        }
-        vt[2 * k] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        vt[2 * k + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t m = __byte_perm(umax_halves(absmax8_bits(vt[2 * k])), umax_halves(absmax8_bits(vt[2 * k + 1])), 0x5410);
+        for (int j = 1; j < 8; ++j) m = absmax_step(m, word_of(v[j], k));
+        m = abs_bits(m);
         m = umax16x2(m, __shfl_xor_sync(0xffffffffu, m, 16));
         if (lane < 16) S.colred[warp][4 * c + k] = m;
       }
@@ -587,22 +611,60 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
 #pragma unroll
         for (int w = 1; w < kQComputeThreads / 32; ++w) m = umax16x2(m, S.colred[w][t >> 1]);
         const Divisor d = group_divisor(S.tab, (t & 1) ? (m >> 16) : (m & 0xFFFFu), p.pow2 != 0);
-        S.coldiv[t] = make_float2(d.s, d.fast ? d.y : -1.0f);
+        S.col_s[t] = d.s;
+        S.col_ny[t] = -d.y;
+        fast = fast && d.fast;
         p.s_t[rb * K + static_cast<int64_t>(kb) * kGroup + t] = d.s;
       }
-      compute_bar();
-      auto shared_divisor = [](float2 sd) {
-        Divisor d;
-        d.s = sd.x;
-        d.y = sd.y;
-        d.fast = sd.y > 0.0f;
-        return d;
-      };
+      // every row and column divisor of the tile on the quotient path, or
+      // IEEE divisions for the whole tile
+      const bool all_fast = compute_bar_and(fast);
+      // Both layouts from one widening per value pair: the row codes with
+      // the row's divisor, the column codes with the two columns' divisors;
+      // an 8x8 byte transpose of the column codes gives, for each column,
+      // its eight codes of rows 8g .. 8g+7: 8 consecutive bytes of X^T.
+      const float4 cs_a = *reinterpret_cast<const float4*>(&S.col_s[8 * c]);
+      const float4 cs_b = *reinterpret_cast<const float4*>(&S.col_s[8 * c + 4]);
+      const float4 cy_a = *reinterpret_cast<const float4*>(&S.col_ny[8 * c]);
+      const float4 cy_b = *reinterpret_cast<const float4*>(&S.col_ny[8 * c + 4]);
+      const float2 cs2[4] = {make_float2(cs_a.x, cs_a.y), make_float2(cs_a.z, cs_a.w), make_float2(cs_b.x, cs_b.y),
+                             make_float2(cs_b.z, cs_b.w)};
+      const float2 cy2[4] = {make_float2(cy_a.x, cy_a.y), make_float2(cy_a.z, cy_a.w), make_float2(cy_b.x, cy_b.y),
+                             make_float2(cy_b.z, cy_b.w)};
+      float2 rd[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = quant8m(v[j], shared_divisor(S.rowdiv[8 * g + j]));
+      for (int j = 0; j < 8; ++j) rd[j] = S.rowdiv[8 * g + j];
+      uint32_t rlo[8], rhi[8];  // row codes of columns 8c .. 8c+3 and 8c+4 .. 8c+7
 #pragma unroll
-      for (int i = 0; i < 8; ++i) stg[8 * c + i][g ^ c] = quant8m(vt[i], shared_divisor(S.coldiv[8 * c + i]));
+      for (int k = 0; k < 4; ++k) {
+        uint32_t rc[8], cc[8];  // row and column code pairs of word k, rows 8g .. 8g+7
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w = word_of(v[j], k);
+          if (all_fast) {
+            const float2 nx = neg_widen(w);
+            rc[j] = quant_pair_nx(nx, make_float2(rd[j].y, rd[j].y), make_float2(rd[j].x, rd[j].x));
+            cc[j] = quant_pair_nx(nx, cy2[k], cs2[k]);
+          } else {
+            rc[j] = quant2_exact_pair(w, rd[j].x, rd[j].x);
+            cc[j] = quant2_exact_pair(w, cs2[k].x, cs2[k].y);
+          }
+          if (k == 0) rlo[j] = rc[j];
+          if (k == 1) rlo[j] = __byte_perm(rlo[j], rc[j], 0x5410);
+          if (k == 2) rhi[j] = rc[j];
+          if (k == 3) rhi[j] = __byte_perm(rhi[j], rc[j], 0x5410);
+        }
+        // pairs of rows interleaved, then the low bytes (column 8c+2k) and
+        // the high bytes (column 8c+2k+1) of the four row pairs
+        uint32_t t4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t4[i] = __byte_perm(cc[2 * i], cc[2 * i + 1], 0x5140);
+        stg[8 * c + 2 * k][g ^ c] = make_uint2(__byte_perm(t4[0], t4[1], 0x5410), __byte_perm(t4[2], t4[3], 0x5410));
+        stg[8 * c + 2 * k + 1][g ^ c] =
+            make_uint2(__byte_perm(t4[0], t4[1], 0x7632), __byte_perm(t4[2], t4[3], 0x7632));
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = make_uint2(rlo[j], rhi[j]);
     }
     // write the staged transposed codes: 8 threads per 128-byte row
     compute_bar();
