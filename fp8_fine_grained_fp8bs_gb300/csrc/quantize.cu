@@ -755,35 +755,28 @@ struct RequantParams {
   int pow2;
 };
 
-// Eight float32 values -> eight codes with one divisor (Markstein quotients
-// as quant_pair; IEEE divisions for a slow divisor; the sign bit of each
-// input ORed into its code to keep the sign of -0).  With a power-of-two
-// divisor on the fast path y = 1/s is exact, so RN(x * y) already is the
-// correctly rounded quotient (and keeps the sign of -0): one multiply.
-__device__ __forceinline__ uint2 quant8f(const float (&v)[8], const Divisor& d, bool pow2) {
+// Eight float32 values, given negated (nv = -x), -> eight codes with one
+// divisor: s and ny = -RN(1/s).  Markstein quotients in the sign-keeping form
+// of quant_pair_nx (a zero input keeps its sign), IEEE divisions for a slow
+// divisor.  With a power-of-two divisor on the fast path 1/s is exact, so
+// RN(nv * ny) already is the correctly rounded quotient: one multiply.
+__device__ __forceinline__ uint2 quant8f_nx(const float (&nv)[8], float s, float ny, bool fast, bool pow2) {
   uint32_t c[4];
-  if (!d.fast) {
+  if (!fast) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      c[j] = d.s == 0.0f ? 0u : e4m3x2(__fdiv_rn(v[2 * j], d.s), __fdiv_rn(v[2 * j + 1], d.s));
+      c[j] = s == 0.0f ? 0u : e4m3x2(__fdiv_rn(-nv[2 * j], s), __fdiv_rn(-nv[2 * j + 1], s));
   } else if (pow2) {
-    const float2 y2 = make_float2(d.y, d.y);
+    const float2 ny2 = make_float2(ny, ny);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 q = __fmul2_rn(make_float2(v[2 * j], v[2 * j + 1]), y2);
+      const float2 q = __fmul2_rn(make_float2(nv[2 * j], nv[2 * j + 1]), ny2);
       c[j] = e4m3x2(q.x, q.y);
     }
   } else {
-    const float2 y2 = make_float2(d.y, d.y), ns2 = make_float2(-d.s, -d.s);
+    const float2 ny2 = make_float2(ny, ny), s2 = make_float2(s, s);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
-      const float2 q0 = __fmul2_rn(a, y2);
-      const float2 r = __ffma2_rn(q0, ns2, a);
-      const float2 q1 = __ffma2_rn(r, y2, q0);
-      c[j] = e4m3x2(q1.x, q1.y) |
-             (__byte_perm(__float_as_uint(v[2 * j]), __float_as_uint(v[2 * j + 1]), 0x0073) & 0x8080u);
-    }
+    for (int j = 0; j < 4; ++j) c[j] = quant_pair_nx(make_float2(nv[2 * j], nv[2 * j + 1]), ny2, s2);
   }
   return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
 }
@@ -795,7 +788,7 @@ __device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
 __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantParams p) {
   griddep_launch_dependents();
   __shared__ float colred[kRqThreads / 32][kGroup];     // per-warp column maxima of |v|
-  __shared__ float2 coldiv[kGroup];                     // per column: (s, RN(1/s)), fast path flag in the sign of y
+  __shared__ float2 coldiv[kGroup];                     // per column: (s, -RN(1/s)); +1 in place of -RN(1/s): IEEE path
   // Output tile: row R of X^T's tile (tile column R) as 16 units of 8 codes;
   // unit u of row R is stored at u ^ (R / 8), so the 8-byte writes of a warp
   // (16 rows R = 8c+i, one unit each) hit 16 different bank pairs.
@@ -817,10 +810,11 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
   };
   load(blockIdx.x, nq, ns);
   for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-    // dequantise: v[i][j] = column i, row j of the thread's 8x8 sub-block
+    // dequantise, negated: v[i][j] = -x of column i, row j of the thread's
+    // 8x8 sub-block (x = code * s_row, so -x = code * -s_row exactly)
     float v[8][8];
     {
-      const float sr[8] = {ns[0].x, ns[0].y, ns[0].z, ns[0].w, ns[1].x, ns[1].y, ns[1].z, ns[1].w};
+      const float sr[8] = {-ns[0].x, -ns[0].y, -ns[0].z, -ns[0].w, -ns[1].x, -ns[1].y, -ns[1].z, -ns[1].w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t w2[2] = {nq[j].x, nq[j].y};
@@ -857,18 +851,14 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_kernel(const RequantPar
 #pragma unroll
       for (int w = 1; w < kRqThreads / 32; ++w) amax = fmaxf(amax, colred[w][t]);
       const Divisor d = divisor_f32(amax, p.pow2 != 0);
-      coldiv[t] = make_float2(d.s, d.fast ? d.y : -1.0f);
+      coldiv[t] = make_float2(d.s, d.fast ? -d.y : 1.0f);
       p.sx_t[rb * p.K + static_cast<int64_t>(kb) * kGroup + t] = d.s;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float2 sd = coldiv[8 * c + i];
-      Divisor d;
-      d.s = sd.x;
-      d.fast = sd.y > 0.0f;
-      d.y = sd.y;
-      stg[8 * c + i][g ^ c] = quant8f(v[i], d, p.pow2 != 0);
+      stg[8 * c + i][g ^ c] = quant8f_nx(v[i], sd.x, sd.y, sd.y < 0.0f, p.pow2 != 0);
     }
     __syncthreads();
     // write the tile out: 8 threads per 128-byte row of X^T
