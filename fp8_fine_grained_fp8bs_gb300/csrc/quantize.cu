@@ -215,6 +215,26 @@ __device__ __forceinline__ uint32_t quant2_exact_pair(uint32_t w, float s0, floa
   return e4m3x2(a, b);
 }
 
+// The quotients of quant_pair_nx, before their conversion.
+__device__ __forceinline__ float2 quot_pair_nx(float2 nx, float2 ny2, float2 s2) {
+  const float2 q0 = __fmul2_rn(nx, ny2);
+  const float2 r = __ffma2_rn(q0, s2, nx);
+  return __ffma2_rn(r, ny2, q0);
+}
+
+// Four float32 -> four E4M3 codes (RNE, saturating) packed in one word, a
+// in the low byte: two conversions written into the two halves of the word.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // Eight consecutive values of one group -> eight codes (byte i = value i).
 __device__ __forceinline__ uint2 quant8m(uint4 v, const Divisor& d) {
   if (!d.fast)
@@ -761,24 +781,28 @@ struct RequantParams {
 // divisor.  With a power-of-two divisor on the fast path 1/s is exact, so
 // RN(nv * ny) already is the correctly rounded quotient: one multiply.
 __device__ __forceinline__ uint2 quant8f_nx(const float (&nv)[8], float s, float ny, bool fast, bool pow2) {
-  uint32_t c[4];
+  float q[8];
   if (!fast) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      c[j] = s == 0.0f ? 0u : e4m3x2(__fdiv_rn(-nv[2 * j], s), __fdiv_rn(-nv[2 * j + 1], s));
+    for (int j = 0; j < 8; ++j) q[j] = s == 0.0f ? 0.0f : __fdiv_rn(-nv[j], s);
   } else if (pow2) {
     const float2 ny2 = make_float2(ny, ny);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 q = __fmul2_rn(make_float2(nv[2 * j], nv[2 * j + 1]), ny2);
-      c[j] = e4m3x2(q.x, q.y);
+      const float2 r = __fmul2_rn(make_float2(nv[2 * j], nv[2 * j + 1]), ny2);
+      q[2 * j] = r.x;
+      q[2 * j + 1] = r.y;
     }
   } else {
     const float2 ny2 = make_float2(ny, ny), s2 = make_float2(s, s);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) c[j] = quant_pair_nx(make_float2(nv[2 * j], nv[2 * j + 1]), ny2, s2);
+    for (int j = 0; j < 4; ++j) {
+      const float2 r = quot_pair_nx(make_float2(nv[2 * j], nv[2 * j + 1]), ny2, s2);
+      q[2 * j] = r.x;
+      q[2 * j + 1] = r.y;
+    }
   }
-  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+  return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
 }
 
 __device__ __forceinline__ Divisor divisor_f32(float a, bool pow2) {
