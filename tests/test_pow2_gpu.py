@@ -118,16 +118,23 @@ def test_requant_pow2_is_lossless_on_gpu():
     assert np.array_equal(vt, oracle.dequantize_1x128(q1, s1).T.astype(np.float64))
 
 
-def test_requant_full_size_sampled():
-    """dY[16384, 2048] of the Wgrad workload, re-tiled at full size; columns sampled for the oracle."""
+@pytest.mark.parametrize("tensor", ["dY_16384x2048", "X_16384x7168"])
+@pytest.mark.parametrize("pow2", [True, False])
+def test_requant_full_size_sampled(tensor, pow2):
+    """The Wgrad workload's dY[16384, 2048] and the benchmark's X[16384, 7168],
+    quantised 1x128 by the oracle and re-tiled at full size (2048 and 7168
+    tiles: every CTA of the grid through several); columns sampled for the
+    oracle (each column's 128x1 groups are independent of the others)."""
     torch, fp8bs = require_gpu()
-    dy, _ = synth.wgrad(0)
-    q1, s1 = oracle.quantize_act_1x128(dy, pow2=True)
-    xq_t, sx_t = fp8bs.requant_1x128_to_128x1(to_dev(q1), to_dev(np.ascontiguousarray(s1.T)), pow2=True)
+    x = synth.wgrad(0)[0] if tensor.startswith("dY") else synth.quantize_input(0)
+    K = x.shape[1]
+    q1, s1 = oracle.quantize_act_1x128(x, pow2=pow2)
+    xq_t, sx_t = fp8bs.requant_1x128_to_128x1(to_dev(q1), to_dev(np.ascontiguousarray(s1.T)), pow2=pow2)
+    assert fp8bs.fp8bs_get_device_status() == 0
     xq_t, sx_t = to_host(xq_t), to_host(sx_t)
-    cols = np.unique(np.concatenate([np.arange(0, 2048, 37), [2047]]))
+    cols = np.unique(np.concatenate([np.arange(0, K, 37), [K - 1]]))
     v = oracle.dequantize_1x128(q1, s1)[:, cols]
-    qt_ref, st_ref = oracle.quantize_act_128x1(v, pow2=True)
+    qt_ref, st_ref = oracle.quantize_act_128x1(v, pow2=pow2)
     assert_bytes_equal(xq_t[cols], qt_ref, "re-tiled codes (sampled columns)")
     assert_scales_equal(sx_t.T[cols], st_ref, "re-tiled scales (sampled columns)")
 
