@@ -331,8 +331,8 @@ struct QShared {
   uint32_t red[2][kQComputeThreads / 32];              // weight: per-warp maxima, by tile parity
   uint32_t colred[kQComputeThreads / 32][kGroup / 2];  // dual: per-warp column maxima, two per word
   float2 rowdiv[kGroup];                               // dual: per row (s, -RN(1/s))
-  float col_s[kGroup];                                 // dual: per column s
-  float col_ny[kGroup];                                // dual: per column -RN(1/s)
+  alignas(16) float col_s[kGroup];                     // dual: per column s (read as float4)
+  alignas(16) float col_ny[kGroup];                    // dual: per column -RN(1/s) (read as float4)
 };
 
 template <int kMode>
