@@ -189,37 +189,28 @@ __device__ __forceinline__ uint32_t quant2_exact(uint32_t w, float s) {
 }
 
 // The BF16 pair w (low half first) widened to float32 and negated: -x is
-// what quant_pair_nx takes.
+// what quot_pair_nx takes.
 __device__ __forceinline__ float2 neg_widen(uint32_t w) {
   return make_float2(__uint_as_float((w << 16) ^ 0x80000000u), __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u));
 }
 
-// Codes of a value pair given as nx = -x, with a divisor per half: s2 the
-// scales, ny2 = -RN(1/s).  The same Markstein quotient as quant_pair with
-// the signs moved: q0 = RN(nx * ny), r = RN(s q0 + nx) = -(x - s q0)
+// Quotients x / s of a value pair given as nx = -x, with a divisor per half:
+// s2 the scales, ny2 = -RN(1/s).  The same Markstein quotient as quant_pair
+// with the signs moved: q0 = RN(nx * ny), r = RN(s q0 + nx) = -(x - s q0)
 // (exact), q1 = RN(q0 + r * ny).  In this form a zero input keeps its sign
 // (x = -0: q0 = -0, r = +0, q1 = -0 + -0 = -0), so no sign restoration
 // follows; every other input gives the same q1 as quant_pair.
-__device__ __forceinline__ uint32_t quant_pair_nx(float2 nx, float2 ny2, float2 s2) {
-  const float2 q0 = __fmul2_rn(nx, ny2);
-  const float2 r = __ffma2_rn(q0, s2, nx);
-  const float2 q1 = __ffma2_rn(r, ny2, q0);
-  return e4m3x2(q1.x, q1.y);
-}
-
-// Codes of the BF16 pair w through IEEE divisions, a scale per half (a
-// zero scale gives a zero code).
-__device__ __forceinline__ uint32_t quant2_exact_pair(uint32_t w, float s0, float s1) {
-  const float a = s0 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w << 16), s0);
-  const float b = s1 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s1);
-  return e4m3x2(a, b);
-}
-
-// The quotients of quant_pair_nx, before their conversion.
 __device__ __forceinline__ float2 quot_pair_nx(float2 nx, float2 ny2, float2 s2) {
   const float2 q0 = __fmul2_rn(nx, ny2);
   const float2 r = __ffma2_rn(q0, s2, nx);
   return __ffma2_rn(r, ny2, q0);
+}
+
+// Quotients of the BF16 pair w through IEEE divisions, a scale per half (a
+// zero scale gives +0, hence a zero code).
+__device__ __forceinline__ float2 quot2_exact(uint32_t w, float s0, float s1) {
+  return make_float2(s0 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w << 16), s0),
+                     s1 == 0.0f ? 0.0f : __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s1));
 }
 
 // Four float32 -> four E4M3 codes (RNE, saturating) packed in one word, a
@@ -269,9 +260,10 @@ __device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
 
 // ---------------------------------------------------------------------------
 // Tile pipeline.  The BF16 input is cut into 128x128 tiles (128 rows of one
-// 128-column block).  A producer warp streams the tiles with TMA into a ring
-// of shared-memory stages; eight compute warps quantise each tile out of
-// shared memory and store codes and scales with coalesced writes.  Loads are
+// 128-column block).  A producer warp (in the dual kernel: compute thread 0)
+// streams the tiles with TMA into a ring of shared-memory stages; eight
+// compute warps quantise each tile out of shared memory and store codes and
+// scales with coalesced writes.  Loads are
 // thereby decoupled from the arithmetic: several tiles per SM are in flight
 // while the warps compute, which a load-then-compute kernel cannot sustain.
 //
@@ -285,9 +277,11 @@ __device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
 //    (i + 4 * half) % 8: the eight lanes of a quarter-warp then read eight
 //    different bank groups.
 //  - block layout (128x1 groups, transposed codes): thread t owns rows
-//    8*(t/16) .. +7 of the 8-column chunk t%16 (an 8x8 sub-block whose
-//    transpose is a byte permutation in registers); the tile is stored
-//    unswizzled and a quarter-warp reads 128 consecutive bytes of a row.
+//    8*(t/16) .. +7 of the 8-column chunk t%16 (an 8x8 sub-block: the dual
+//    kernel packs each column's codes straight from its quotients, the
+//    weight's transposed copy is a byte permutation of the row codes in
+//    registers); the tile is stored unswizzled and a quarter-warp reads 128
+//    consecutive bytes of a row.
 enum TileMode : int {
   kModeAct = 0,      // 1x128 groups, row layout
   kModeWeight = 1,   // one 128x128 group per tile, row layout
@@ -308,6 +302,12 @@ struct QCfg {
 
 constexpr int kQComputeThreads = 256;
 constexpr int kQThreads = kQComputeThreads + 32;  // + the producer warp
+// Threads of a launch.  The dual kernel has no producer warp: its thread 0
+// issues the loads, so two CTAs of 8 warps (16 per SM, 4 per scheduler)
+// leave each thread 128 registers, which both layouts' quotients of a
+// sub-block need; 18 warps would leave 96.
+template <int kMode>
+constexpr int q_threads() { return kMode == kModeDual ? kQComputeThreads : kQThreads; }
 constexpr int kTileBytes = kGroup * kGroup * 2;    // 32 KB of BF16
 constexpr int kTileRowBytes = kGroup * 2;
 constexpr int kQMaxStages = 3;
@@ -384,7 +384,7 @@ __device__ __forceinline__ void quant_row64(const uint32_t (&w)[32], const Divis
 // kModeActWeight they are followed by pw's tensor (through tmw), quantised
 // in 128x128 groups.  Other modes ignore tmw and pw.
 template <int kMode>
-__global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
+__global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                       const TileParams p, const TileParams pw) {
   using Q = QCfg<kMode>;
@@ -413,6 +413,24 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
   }
   div_table_init(S.tab);
   __syncthreads();
+  // The dual kernel's loads: thread 0 fills the ring here and refills a
+  // stage once every thread has passed the tile's first barrier (all have
+  // read the stage by then); it counts the loads it issued and the tiles it
+  // saw land, so that after a timeout it waits for the copies still in flight.
+  constexpr bool kInline = kMode == kModeDual;
+  int issued_inline = 0, consumed_inline = 0;
+  if (kInline && threadIdx.x == 0) {
+    prefetch_tmap(&tmx);
+    for (int i = 0; i < Q::kStages; ++i) {
+      const int64_t tile = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+      if (tile >= ntiles) break;
+      const int64_t rb0 = tile / p.nkb;
+      const int kb0 = static_cast<int>(tile - rb0 * p.nkb);
+      mbar_arrive_expect_tx(&S.full[i], kTileBytes);
+      tma_load_2d(tiles + i * kTileBytes, &tmx, &S.full[i], kb0 * kGroup, static_cast<int>(rb0 * kGroup));
+      ++issued_inline;
+    }
+  }
 
   if (warp == kQComputeThreads / 32) {
     // ------------------------------------------------------------ producer
@@ -486,6 +504,8 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       if (kb >= p.nkb) { kb -= p.nkb; ++rb; }
     }
     const bool ok = mbar_wait(&S.full[s], ph, p.timeout_ns);
+    if (kInline && threadIdx.x == 0 && ok) ++consumed_inline;
+    const int cur_s = s;
     const uint8_t* stage = tiles + s * kTileBytes;
 
     if (Q::kRowLayout) {
@@ -554,7 +574,7 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
     const int64_t c0 = static_cast<int64_t>(kb) * kGroup + 8 * c;  // and first column
     // the tile is in registers: hand the stage back to the producer
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (!kInline && lane == 0) mbar_arrive(&S.empty[s]);
     if (++s == Q::kStages) { s = 0; ph ^= 1u; }
 
     if (kMode == kModeWeightT) {
@@ -626,6 +646,18 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
         if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
         break;
       }
+      // every thread has read this tile's stage: refill it
+      if (kInline && t == 0) {
+        const int64_t next = tile + static_cast<int64_t>(Q::kStages) * gridDim.x;
+        if (next < ntiles) {
+          const int64_t rbn = next / p.nkb;
+          const int kbn = static_cast<int>(next - rbn * p.nkb);
+          mbar_arrive_expect_tx(&S.full[cur_s], kTileBytes);
+          tma_load_2d(tiles + cur_s * kTileBytes, &tmx, &S.full[cur_s], kbn * kGroup,
+                      static_cast<int>(rbn * kGroup));
+          ++issued_inline;
+        }
+      }
       if (t < kGroup) {  // one divisor per column
         uint32_t m = S.colred[0][t >> 1];
 #pragma unroll
@@ -639,10 +671,12 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       // every row and column divisor of the tile on the quotient path, or
       // IEEE divisions for the whole tile
       const bool all_fast = compute_bar_and(fast);
-      // Both layouts from one widening per value pair: the row codes with
-      // the row's divisor, the column codes with the two columns' divisors;
-      // an 8x8 byte transpose of the column codes gives, for each column,
-      // its eight codes of rows 8g .. 8g+7: 8 consecutive bytes of X^T.
+      // Both layouts from one widening per value pair: the row quotients
+      // with the row's divisor, the column quotients with the two columns'
+      // divisors.  A row's codes are its quotients in order; the codes of
+      // column 8c+2k for rows 8g+4jg .. +3 are the low halves of those rows'
+      // column quotients of word k (the high halves: column 8c+2k+1), four
+      // conversions packed into one word, so no byte transposes follow.
       const float4 cs_a = *reinterpret_cast<const float4*>(&S.col_s[8 * c]);
       const float4 cs_b = *reinterpret_cast<const float4*>(&S.col_s[8 * c + 4]);
       const float4 cy_a = *reinterpret_cast<const float4*>(&S.col_ny[8 * c]);
@@ -651,40 +685,37 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
                              make_float2(cs_b.z, cs_b.w)};
       const float2 cy2[4] = {make_float2(cy_a.x, cy_a.y), make_float2(cy_a.z, cy_a.w), make_float2(cy_b.x, cy_b.y),
                              make_float2(cy_b.z, cy_b.w)};
-      float2 rd[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) rd[j] = S.rowdiv[8 * g + j];
-      uint32_t rlo[8], rhi[8];  // row codes of columns 8c .. 8c+3 and 8c+4 .. 8c+7
+      for (int jg = 0; jg < 2; ++jg) {  // rows 8g+4jg .. 8g+4jg+3
+        float2 cq[4][4];                // column quotients [row][word]
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t rc[8], cc[8];  // row and column code pairs of word k, rows 8g .. 8g+7
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * jg + jj;
+          const float2 rd = S.rowdiv[8 * g + j];
+          float2 rq[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w = word_of(v[j], k);
-          if (all_fast) {
-            const float2 nx = neg_widen(w);
-            rc[j] = quant_pair_nx(nx, make_float2(rd[j].y, rd[j].y), make_float2(rd[j].x, rd[j].x));
-            cc[j] = quant_pair_nx(nx, cy2[k], cs2[k]);
-          } else {
-            rc[j] = quant2_exact_pair(w, rd[j].x, rd[j].x);
-            cc[j] = quant2_exact_pair(w, cs2[k].x, cs2[k].y);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t w = word_of(v[j], k);
+            if (all_fast) {
+              const float2 nx = neg_widen(w);
+              rq[k] = quot_pair_nx(nx, make_float2(rd.y, rd.y), make_float2(rd.x, rd.x));
+              cq[jj][k] = quot_pair_nx(nx, cy2[k], cs2[k]);
+            } else {
+              rq[k] = quot2_exact(w, rd.x, rd.x);
+              cq[jj][k] = quot2_exact(w, cs2[k].x, cs2[k].y);
+            }
           }
-          if (k == 0) rlo[j] = rc[j];
-          if (k == 1) rlo[j] = __byte_perm(rlo[j], rc[j], 0x5410);
-          if (k == 2) rhi[j] = rc[j];
-          if (k == 3) rhi[j] = __byte_perm(rhi[j], rc[j], 0x5410);
+          *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) =
+              make_uint2(e4m3x4(rq[0].x, rq[0].y, rq[1].x, rq[1].y), e4m3x4(rq[2].x, rq[2].y, rq[3].x, rq[3].y));
         }
-        // pairs of rows interleaved, then the low bytes (column 8c+2k) and
-        // the high bytes (column 8c+2k+1) of the four row pairs
-        uint32_t t4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) t4[i] = __byte_perm(cc[2 * i], cc[2 * i + 1], 0x5140);
-        stg[8 * c + 2 * k][g ^ c] = make_uint2(__byte_perm(t4[0], t4[1], 0x5410), __byte_perm(t4[2], t4[3], 0x5410));
-        stg[8 * c + 2 * k + 1][g ^ c] =
-            make_uint2(__byte_perm(t4[0], t4[1], 0x7632), __byte_perm(t4[2], t4[3], 0x7632));
+        for (int k = 0; k < 4; ++k) {
+          reinterpret_cast<uint32_t*>(&stg[8 * c + 2 * k][g ^ c])[jg] =
+              e4m3x4(cq[0][k].x, cq[1][k].x, cq[2][k].x, cq[3][k].x);
+          reinterpret_cast<uint32_t*>(&stg[8 * c + 2 * k + 1][g ^ c])[jg] =
+              e4m3x4(cq[0][k].y, cq[1][k].y, cq[2][k].y, cq[3][k].y);
+        }
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = make_uint2(rlo[j], rhi[j]);
     }
     // write the staged transposed codes: 8 threads per 128-byte row
     compute_bar();
@@ -697,6 +728,10 @@ __global__ void __launch_bounds__(kQThreads, QCfg<kMode>::kMinBlocks)
       const int kl = k ^ (cr >> 1);  // logical 16-byte chunk of the row
       *reinterpret_cast<uint4*>(p.q_t + (static_cast<int64_t>(kb) * kGroup + R) * p.rows + rb * kGroup + 16 * kl) = w;
     }
+  }
+  if (kInline && threadIdx.x == 0) {
+    for (int i = consumed_inline; i < issued_inline; ++i)
+      (void)mbar_wait(&S.full[i % Q::kStages], (i / Q::kStages) & 1u, p.timeout_ns);
   }
 }
 
@@ -740,14 +775,15 @@ cudaError_t launch_tiles(const uint16_t* x, int64_t ld, const TileParams& p, int
   static std::atomic<int> per_sm_cache[kMaxCachedDevices];  // co-resident CTAs per SM, per device
   int per_sm = 0;
   e = cached_per_device(
-      per_sm_cache, [&](int* n) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, kQThreads, smem); },
+      per_sm_cache,
+      [&](int* n) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, q_threads<kMode>(), smem); },
       &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
   const int grid = static_cast<int>(ntiles < slots ? ntiles : slots);
   TileParams none = p;
   none.nrb = 0;
-  kern<<<grid, kQThreads, smem, stream>>>(map, map_w, p, pw != nullptr ? *pw : none);
+  kern<<<grid, q_threads<kMode>(), smem, stream>>>(map, map_w, p, pw != nullptr ? *pw : none);
   return cudaGetLastError();
 }
 
@@ -777,7 +813,7 @@ struct RequantParams {
 
 // Eight float32 values, given negated (nv = -x), -> eight codes with one
 // divisor: s and ny = -RN(1/s).  Markstein quotients in the sign-keeping form
-// of quant_pair_nx (a zero input keeps its sign), IEEE divisions for a slow
+// of quot_pair_nx (a zero input keeps its sign), IEEE divisions for a slow
 // divisor.  With a power-of-two divisor on the fast path 1/s is exact, so
 // RN(nv * ny) already is the correctly rounded quotient: one multiply.
 __device__ __forceinline__ uint2 quant8f_nx(const float (&nv)[8], float s, float ny, bool fast, bool pow2) {
