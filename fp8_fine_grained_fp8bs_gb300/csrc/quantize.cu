@@ -242,30 +242,14 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
   return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
-// Column i (0..7) of an 8x8 byte tile held as 8 rows of 8 bytes: byte j of
-// the result is byte i of row j.
-__device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
-  const int wsel = i >> 2;
-  const uint32_t b = static_cast<uint32_t>(i & 3);
-  const uint32_t sel = b | ((b + 4) << 4);  // byte b of the first word, byte b of the second
-  uint32_t p[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t x0 = wsel ? q[2 * j].y : q[2 * j].x;
-    const uint32_t x1 = wsel ? q[2 * j + 1].y : q[2 * j + 1].x;
-    p[j] = __byte_perm(x0, x1, sel);
-  }
-  return make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
-}
-
 // ---------------------------------------------------------------------------
 // Tile pipeline.  The BF16 input is cut into 128x128 tiles (128 rows of one
-// 128-column block).  A producer warp (in the dual kernel: compute thread 0)
-// streams the tiles with TMA into a ring of shared-memory stages; eight
-// compute warps quantise each tile out of shared memory and store codes and
-// scales with coalesced writes.  Loads are
-// thereby decoupled from the arithmetic: several tiles per SM are in flight
-// while the warps compute, which a load-then-compute kernel cannot sustain.
+// 128-column block).  A producer warp (in the block-layout kernels: compute
+// thread 0) streams the tiles with TMA into a ring of shared-memory stages;
+// eight compute warps quantise each tile out of shared memory and store codes
+// and scales with coalesced writes.  Loads are thereby decoupled from the
+// arithmetic: several tiles per SM are in flight while the warps compute,
+// which a load-then-compute kernel cannot sustain.
 //
 // Two thread layouts:
 //  - row layout (1x128 groups, and weights without the transposed copy):
@@ -277,11 +261,10 @@ __device__ __forceinline__ uint2 byte_column(const uint2 (&q)[8], int i) {
 //    (i + 4 * half) % 8: the eight lanes of a quarter-warp then read eight
 //    different bank groups.
 //  - block layout (128x1 groups, transposed codes): thread t owns rows
-//    8*(t/16) .. +7 of the 8-column chunk t%16 (an 8x8 sub-block: the dual
-//    kernel packs each column's codes straight from its quotients, the
-//    weight's transposed copy is a byte permutation of the row codes in
-//    registers); the tile is stored unswizzled and a quarter-warp reads 128
-//    consecutive bytes of a row.
+//    8*(t/16) .. +7 of the 8-column chunk t%16 (an 8x8 sub-block whose
+//    column codes are packed straight from the quotients, no transposes);
+//    the tile is stored unswizzled and a quarter-warp reads 128 consecutive
+//    bytes of a row.
 enum TileMode : int {
   kModeAct = 0,      // 1x128 groups, row layout
   kModeWeight = 1,   // one 128x128 group per tile, row layout
@@ -302,12 +285,15 @@ struct QCfg {
 
 constexpr int kQComputeThreads = 256;
 constexpr int kQThreads = kQComputeThreads + 32;  // + the producer warp
-// Threads of a launch.  The dual kernel has no producer warp: its thread 0
-// issues the loads, so two CTAs of 8 warps (16 per SM, 4 per scheduler)
-// leave each thread 128 registers, which both layouts' quotients of a
-// sub-block need; 18 warps would leave 96.
+// Threads of a launch.  The block-layout kernels (dual, weight with the
+// transposed copy) have no producer warp: their thread 0 issues the loads,
+// so two CTAs of 8 warps (16 per SM, 4 per scheduler) leave each thread 128
+// registers, which the quotients of a sub-block's two layouts need; 18 warps
+// would leave 96.
 template <int kMode>
-constexpr int q_threads() { return kMode == kModeDual ? kQComputeThreads : kQThreads; }
+constexpr bool q_inline_loads() { return kMode == kModeDual || kMode == kModeWeightT; }
+template <int kMode>
+constexpr int q_threads() { return q_inline_loads<kMode>() ? kQComputeThreads : kQThreads; }
 constexpr int kTileBytes = kGroup * kGroup * 2;    // 32 KB of BF16
 constexpr int kTileRowBytes = kGroup * 2;
 constexpr int kQMaxStages = 3;
@@ -413,11 +399,11 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
   }
   div_table_init(S.tab);
   __syncthreads();
-  // The dual kernel's loads: thread 0 fills the ring here and refills a
+  // Block-layout kernels' loads: thread 0 fills the ring here and refills a
   // stage once every thread has passed the tile's first barrier (all have
   // read the stage by then); it counts the loads it issued and the tiles it
   // saw land, so that after a timeout it waits for the copies still in flight.
-  constexpr bool kInline = kMode == kModeDual;
+  constexpr bool kInline = q_inline_loads<kMode>();
   int issued_inline = 0, consumed_inline = 0;
   if (kInline && threadIdx.x == 0) {
     prefetch_tmap(&tmx);
@@ -577,6 +563,21 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
     if (!kInline && lane == 0) mbar_arrive(&S.empty[s]);
     if (++s == Q::kStages) { s = 0; ph ^= 1u; }
 
+    // thread 0 of a block-layout kernel: load the CTA's tile kStages ahead
+    // into the stage this tile came from
+    auto refill = [&]() {
+      if (kInline && t == 0) {
+        const int64_t next = tile + static_cast<int64_t>(Q::kStages) * gridDim.x;
+        if (next < ntiles) {
+          const int64_t rbn = next / p.nkb;
+          const int kbn = static_cast<int>(next - rbn * p.nkb);
+          mbar_arrive_expect_tx(&S.full[cur_s], kTileBytes);
+          tma_load_2d(tiles + cur_s * kTileBytes, &tmx, &S.full[cur_s], kbn * kGroup,
+                      static_cast<int>(rbn * kGroup));
+          ++issued_inline;
+        }
+      }
+    };
     if (kMode == kModeWeightT) {
       uint32_t m = 0;
 #pragma unroll
@@ -589,6 +590,7 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
         if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
         break;
       }
+      refill();
       uint32_t a = S.red[par][0];
 #pragma unroll
       for (int i = 1; i < kQComputeThreads / 32; ++i) a = max(a, S.red[par][i]);
@@ -597,15 +599,27 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
         p.s[rb * p.nkb + kb] = d.s;
         p.s_t[static_cast<int64_t>(kb) * p.nrb + rb] = d.s;
       }
-      uint2 q[8];
+      // one scale for the block: the codes of W^T are the same quotients,
+      // packed by column
+      const float2 ny2 = make_float2(-d.y, -d.y), s2 = make_float2(d.s, d.s);
+      float2 q[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        q[j] = quant8m(v[j], d);
-        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = q[j];
-      }
-      // one scale for the block: the codes of W^T are the transposed codes
 #pragma unroll
-      for (int i = 0; i < 8; ++i) stg[8 * c + i][g ^ c] = byte_column(q, i);
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w = word_of(v[j], k);
+          q[j][k] = d.fast ? quot_pair_nx(neg_widen(w), ny2, s2) : quot2_exact(w, d.s, d.s);
+        }
+        *reinterpret_cast<uint2*>(p.q + (r0 + j) * K + c0) = make_uint2(
+            e4m3x4(q[j][0].x, q[j][0].y, q[j][1].x, q[j][1].y), e4m3x4(q[j][2].x, q[j][2].y, q[j][3].x, q[j][3].y));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        stg[8 * c + 2 * k][g ^ c] = make_uint2(e4m3x4(q[0][k].x, q[1][k].x, q[2][k].x, q[3][k].x),
+                                               e4m3x4(q[4][k].x, q[5][k].x, q[6][k].x, q[7][k].x));
+        stg[8 * c + 2 * k + 1][g ^ c] = make_uint2(e4m3x4(q[0][k].y, q[1][k].y, q[2][k].y, q[3][k].y),
+                                                   e4m3x4(q[4][k].y, q[5][k].y, q[6][k].y, q[7][k].y));
+      }
     } else {
       // dual: 1x128 groups, row 8g+j reducing over the 16 threads of a
       // half-warp (the maxima of rows 2i and 2i+1 travel packed in one word)
@@ -646,18 +660,7 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
         if (t == 0) atomicCAS(&g_quant_status, 0, kStatusTimeout);
         break;
       }
-      // every thread has read this tile's stage: refill it
-      if (kInline && t == 0) {
-        const int64_t next = tile + static_cast<int64_t>(Q::kStages) * gridDim.x;
-        if (next < ntiles) {
-          const int64_t rbn = next / p.nkb;
-          const int kbn = static_cast<int>(next - rbn * p.nkb);
-          mbar_arrive_expect_tx(&S.full[cur_s], kTileBytes);
-          tma_load_2d(tiles + cur_s * kTileBytes, &tmx, &S.full[cur_s], kbn * kGroup,
-                      static_cast<int>(rbn * kGroup));
-          ++issued_inline;
-        }
-      }
+      refill();  // every thread has read this tile's stage
       if (t < kGroup) {  // one divisor per column
         uint32_t m = S.colred[0][t >> 1];
 #pragma unroll
