@@ -558,9 +558,9 @@ __global__ void __launch_bounds__(q_threads<kMode>(), QCfg<kMode>::kMinBlocks)
       v[j] = ok ? *reinterpret_cast<const uint4*>(src + j * kTileRowBytes) : make_uint4(0u, 0u, 0u, 0u);
     const int64_t r0 = rb * kGroup + 8 * g;                        // this thread's first row
     const int64_t c0 = static_cast<int64_t>(kb) * kGroup + 8 * c;  // and first column
-    // the tile is in registers: hand the stage back to the producer
-    __syncwarp();
-    if (!kInline && lane == 0) mbar_arrive(&S.empty[s]);
+    // the tile is in registers; its stage is refilled once every thread has
+    // passed the tile's first barrier (refill below)
+    static_assert(Q::kRowLayout || kInline, "the block layouts load in-kernel");
     if (++s == Q::kStages) { s = 0; ph ^= 1u; }
 
     // thread 0 of a block-layout kernel: load the CTA's tile kStages ahead
